@@ -1,0 +1,188 @@
+/*
+ * kvq.h -- C ABI of libkvq, a quantized paged KV cache for one GB300 GPU.
+ *
+ * Two hot operations, both hand-written CUDA for sm_103a:
+ *
+ *   kvq_cache_write       new bf16 K/V vectors -> scale -> FP8 E4M3 / packed
+ *                         INT4 / BF16 codes -> scatter into paged blocks.
+ *   kvq_decode_attention  paged GQA decode over that cache, K scale folded
+ *                         into the QK product, V scale into the PV sum.
+ *
+ * The operations and their scale layouts follow three pages:
+ *   [P1] "Per-tensor vs per-head FP8 KV cache scales"
+ *   [P2] "Per-token-head KV cache scale overhead"
+ *   [P3] "FP8 KV cache layer skipping vs per-head scales"
+ *
+ * Conventions for every call:
+ *  - Pointers named *_cache, q, out, k_new, v_new, slot_mapping, block_table,
+ *    context_lens, workspace and the scale arrays are DEVICE pointers owned by
+ *    the caller; the library never allocates, frees or retains them.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Device work is enqueued asynchronously on it; a call returns
+ *    once the work is enqueued.
+ *  - Argument errors are detected on the host before anything is launched and
+ *    reported as a kvq_status; nothing is launched in that case.  Index errors
+ *    found on the device (a slot or block id outside the cache, a negative
+ *    context length) skip the bad access and set a device error word that
+ *    kvq_get_device_error() reads.  No call falls back to another path.
+ *  - kvq_ctx is host-only configuration; it may be shared between threads
+ *    for the read-only calls below.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size or layer index */
+  KVQ_ERR_UNSUPPORTED = 2,  /* head_dim, block_size, mode or GQA ratio not built */
+  KVQ_ERR_ALIGNMENT = 3,    /* a pointer or stride breaks the 16-byte rule */
+  KVQ_ERR_WORKSPACE = 4,    /* workspace missing or smaller than kvq_decode_plan says */
+  KVQ_ERR_CUDA = 5,         /* a CUDA launch or query failed */
+  KVQ_ERR_BAD_INDEX = 6,    /* device saw a slot / block id outside the cache */
+  KVQ_ERR_TIMEOUT = 7       /* a bounded device wait gave up */
+} kvq_status;
+
+/* Cache dtype and scale layout of one layer ([P1] "Per-tensor vs per-head FP8
+ * KV cache scales"; [P2] "INT4 makes the metadata fraction larger"; [P3] "FP8
+ * KV cache layer skipping vs per-head scales"). */
+typedef enum kvq_mode {
+  KVQ_BF16 = 0,                /* skipped layer: native bf16, no scales */
+  KVQ_FP8_PER_TENSOR = 1,      /* E4M3, one K and one V scale per layer */
+  KVQ_FP8_PER_HEAD = 2,        /* E4M3, static scale per KV head */
+  KVQ_FP8_PER_TOKEN_HEAD = 3,  /* E4M3, scale = amax/448 per token and head */
+  KVQ_INT4_PER_TOKEN_HEAD = 4  /* packed symmetric INT4, scale = amax/7 */
+} kvq_mode;
+
+/* Model/cache description, the pages' statement of the problem: layers, Hq,
+ * Hkv, head size, block size, per-layer scale mode, window and skipped
+ * (KVQ_BF16) layers. */
+typedef struct kvq_config {
+  int num_layers;
+  int num_q_heads;          /* Hq; a multiple of num_kv_heads, Hq/Hkv <= 16 */
+  int num_kv_heads;         /* Hkv */
+  int head_dim;             /* D: 64, 128 or 256 */
+  int block_size;           /* tokens per block: 16, 32, 64 or 128 */
+  long long num_blocks;     /* blocks in each layer's cache */
+  const int* layer_mode;    /* host [num_layers] of kvq_mode; copied by kvq_create */
+  const int* layer_window;  /* host [num_layers]; 0 = full attention, W > 0 keeps
+                               the last W positions; NULL = all full */
+  float softmax_scale;      /* 0 => 1/sqrt(head_dim) */
+} kvq_config;
+
+typedef struct kvq_ctx kvq_ctx;
+
+/* Validates and copies *cfg.  Host only; no CUDA call. */
+kvq_status kvq_create(const kvq_config* cfg, kvq_ctx** out);
+void kvq_destroy(kvq_ctx* ctx);
+
+/* Bytes of one layer's K code buffer and K scale buffer (V is the same).
+ * Codes: [num_blocks][Hkv][block_size][row] with row = 2D (BF16), D (FP8) or
+ * D/2 (INT4) bytes.  Scales (dynamic modes only, else 0): [num_blocks][Hkv]
+ * [block_size] fp32.  Each (block, head) page of codes and of scales is
+ * contiguous.  Host only. */
+kvq_status kvq_layer_buffer_sizes(const kvq_ctx* ctx, int layer, size_t* code_bytes,
+                                  size_t* scale_bytes);
+
+/* Capacity accounting for one sequence of `context_tokens` positions.
+ * Payload 2 x Hkv x D x bytes/elem per layer and retained token, dynamic
+ * scales 2 x Hkv x 4 bytes ([P2] "Per-token-head KV cache scale overhead"),
+ * static scales 8 bytes per per-tensor layer and 8 x Hkv per per-head layer
+ * ([P1] "Static per-head metadata is almost free"), window layers retain
+ * min(context, W) positions ([P3] "Layer skipping follows retained-token
+ * footprint"), block bytes = per-token bytes x block size ([P2] "Convert
+ * bytes into block capacity").  Bytes are before allocator rounding. */
+typedef struct kvq_capacity {
+  double payload_bytes_per_token;   /* all layers, codes only */
+  double scale_bytes_per_token;     /* all layers, dynamic scales only */
+  double bytes_per_token;           /* payload + scales */
+  double block_bytes;               /* bytes_per_token x block_size */
+  long long retained_positions;     /* sum over layers of retained positions */
+  long long static_scale_bytes;     /* per-tensor and per-head scale arrays */
+  double cache_bytes;               /* retained codes + scales + static scales */
+  double bf16_cache_bytes;          /* the same retention with every layer BF16 */
+} kvq_capacity;
+kvq_status kvq_cache_bytes(const kvq_ctx* ctx, long long context_tokens, kvq_capacity* out);
+
+/* Fused quantize-and-scatter of num_tokens new K/V vectors into `layer`.
+ *
+ * k_new, v_new: bf16 [num_tokens][Hkv][D], token t starting at element
+ *   t * kv_token_stride (0 => Hkv*D); 16-byte aligned, stride a multiple of 8.
+ * slot_mapping: int64 [num_tokens]; token t goes to block slot/block_size,
+ *   offset slot%block_size; slot < 0 skips the token (padding).
+ * k_scale, v_scale: fp32, [1] for KVQ_FP8_PER_TENSOR, [Hkv] for
+ *   KVQ_FP8_PER_HEAD, ignored (may be NULL) otherwise.
+ * k_cache, v_cache: the layer's code buffers (16-byte aligned).
+ * k_cache_scale, v_cache_scale: the layer's scale buffers for the dynamic
+ *   modes, ignored (may be NULL) otherwise.
+ * Per element: y = x / s rounded to fp32, then E4M3 round-to-nearest-even
+ * with saturation to +-448, or INT4 q = clamp(rint(y), -7, 7) packed two per
+ * byte (even element in the low nibble).  Dynamic scales: s = amax/448 (FP8)
+ * or amax/7 (INT4) in fp32, s = 1 when amax = 0 ([P1] "Dynamic per-token-head
+ * scales add 3.125 percent"; [P2] "INT4 makes the metadata fraction larger").
+ * A slot past the cache skips the token and sets KVQ_ERR_BAD_INDEX on the
+ * device word. */
+kvq_status kvq_cache_write(const kvq_ctx* ctx, int layer, const void* k_new, const void* v_new,
+                           long long kv_token_stride, const long long* slot_mapping,
+                           long long num_tokens, const float* k_scale, const float* v_scale,
+                           void* k_cache, void* v_cache, float* k_cache_scale,
+                           float* v_cache_scale, void* stream);
+
+/* Static per-head calibration: scale_out[h] = amax over a bf16 sample
+ * x [num_tokens][Hkv][D] of head h, divided by qmax (448 for E4M3) in fp32;
+ * 1.0 for an all-zero head ([P1] "Calibration changes which scale layout
+ * exists": an online maximum stands in for warm-up calibration).
+ * scale_out: device fp32 [Hkv], overwritten. */
+kvq_status kvq_calibrate_per_head(const kvq_ctx* ctx, const void* x, long long num_tokens,
+                                  float qmax, float* scale_out, void* stream);
+
+/* Split-K plan for a decode call: the split count used when the caller
+ * passes num_splits = 0 (from the batch, KV heads, longest context and the
+ * device's SM count) and the workspace bytes a call with that split count
+ * needs.  On input *num_splits may hold a requested count (>0) to size. */
+kvq_status kvq_decode_plan(const kvq_ctx* ctx, int layer, int batch, int max_context,
+                           int* num_splits, size_t* workspace_bytes);
+
+/* Paged decode attention, one query token per sequence.
+ *
+ * q: bf16 [batch][Hq][D], 16-byte aligned.  Query head hq reads KV head
+ *   hq / (Hq/Hkv).
+ * block_table: int32 [batch][max_blocks_per_seq]; entries for positions that
+ *   are not read may hold anything (e.g. -1).
+ * context_lens: int32 [batch]; L counts the current token, whose K/V were
+ *   written first.  The query attends to positions [lo, L), lo = max(0, L-W)
+ *   for a window W, else 0.  L = 0 gives a zero output row.
+ * out: fp32 [batch][Hq][D] = sum_p softmax(softmax_scale <q, K_hat[p]>) V_hat[p]
+ *   with K_hat = code x K scale, V_hat = code x V scale.
+ * num_splits: >= 1 splits of each sequence's positions, merged by
+ *   log-sum-exp; 0 = the plan's choice.  With more than one split the
+ *   partials go to `workspace` (kvq_decode_plan gives its size).
+ * Scale pointers as for kvq_cache_write. */
+kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
+                                const void* k_cache, const void* v_cache, const float* k_scale,
+                                const float* v_scale, const float* k_cache_scale,
+                                const float* v_cache_scale, const int* block_table,
+                                int max_blocks_per_seq, const int* context_lens, int batch,
+                                int max_context, float* out, int num_splits, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* The device codec on its own: out[i] = E4M3 code of in[i] (RNE, saturating
+ * to +-448), exactly as kvq_cache_write encodes y.  in: device fp32 [n],
+ * out: device uint8 [n]. */
+kvq_status kvq_e4m3_encode(const float* in, unsigned char* out, long long n, void* stream);
+
+/* Synchronizes `stream`, returns the device error word of the current device
+ * as a status (KVQ_OK, KVQ_ERR_BAD_INDEX or KVQ_ERR_TIMEOUT) and clears it. */
+kvq_status kvq_get_device_error(void* stream);
+
+const char* kvq_status_string(kvq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H_ */

@@ -1,0 +1,67 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvq {
+
+enum Mode { BF16 = 0, FP8_PER_TENSOR = 1, FP8_PER_HEAD = 2, FP8_PER_TOKEN_HEAD = 3,
+            INT4_PER_TOKEN_HEAD = 4 };
+
+// Device error word bits.
+enum : unsigned { ERR_BAD_INDEX = 1u, ERR_TIMEOUT = 2u };
+
+struct WriteArgs {
+  const uint16_t* k_new;       // bf16 bits
+  const uint16_t* v_new;
+  long long token_stride;      // elements between tokens
+  const long long* slots;
+  long long T;
+  int Hkv;
+  int bs;
+  long long num_blocks;
+  const float* k_scale;        // static modes
+  const float* v_scale;
+  uint8_t* k_cache;
+  uint8_t* v_cache;
+  float* k_cs;                 // dynamic modes
+  float* v_cs;
+  unsigned* err;
+};
+
+struct DecodeArgs {
+  const uint16_t* q;           // bf16 [B][Hq][D]
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const float* k_scale;        // static modes: [1] or [Hkv]
+  const float* v_scale;
+  const float* k_cs;           // dynamic modes: [num_blocks][Hkv][bs]
+  const float* v_cs;
+  const int* block_table;      // [B][max_blocks]
+  const int* context_lens;     // [B]
+  float* out;                  // [B][Hq][D]
+  float* ws_o;                 // [B][Hkv][S][G][D] unnormalised partial outputs
+  float* ws_ml;                // [B][Hkv][S][G][2] running max (log2 units) and sum
+  unsigned* err;
+  int B, Hq, Hkv, bs, max_blocks, window, splits;
+  long long num_blocks;
+  float qk_scale;              // softmax_scale * log2(e)
+};
+
+// Launchers (return cudaGetLastError() of the launch).
+cudaError_t launch_cache_write(int mode, int D, const WriteArgs& a, cudaStream_t st);
+cudaError_t launch_calibrate(const uint16_t* x, long long T, int Hkv, int D, float qmax,
+                             float* out, cudaStream_t st);
+cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, long long n, cudaStream_t st);
+// Returns cudaErrorInvalidValue for an unsupported (mode, D, G) combination.
+cudaError_t launch_decode(int mode, int D, int G, const DecodeArgs& a, cudaStream_t st);
+bool decode_supported(int mode, int D, int G);
+
+// Device error word of the current device.
+unsigned* error_word();
+
+int sm_count();
+
+}  // namespace kvq

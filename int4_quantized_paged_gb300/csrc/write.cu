@@ -1,0 +1,233 @@
+// Fused quantize-and-scatter cache write, static per-head calibration and the
+// stand-alone E4M3 encoder.
+//
+// Scale layouts: "Per-tensor vs per-head FP8 KV cache scales" (sections
+// "Per-tensor vs per-head FP8 KV cache scales" and "Dynamic per-token-head
+// scales add 3.125 percent"); packed INT4: "Per-token-head KV cache scale
+// overhead", section "INT4 makes the metadata fraction larger".
+//
+// The write is a pure HBM stream: per token and KV head it reads 2*2D bytes
+// of bf16 K/V and writes 2*D*elem code bytes plus 8 scale bytes.  One group of
+// D/8 lanes owns one head vector (16-byte loads, 8 bf16 per lane); the amax is
+// a shuffle reduction inside the group.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+
+__device__ unsigned g_error_word;
+
+unsigned* error_word() {
+  static unsigned* ptr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return ptr[dev];
+}
+
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 -> two E4M3 codes, round to nearest even, saturating to +-448
+// (hardware cvt with .satfinite).  `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t int4_code(float y) {
+  int q = __float2int_rn(y);              // round to nearest even
+  q = max(-7, min(7, q));
+  return (uint32_t)q & 0xFu;
+}
+
+// Max over the LPV lanes of one vector group.  Groups of one warp may take
+// different paths (a skipped slot, the end of the grid-stride loop), so the
+// shuffle names only the group's own lanes.
+template <int LPV>
+__device__ __forceinline__ float group_max(float v) {
+  const unsigned lane = threadIdx.x & 31u;
+  const unsigned mask = (LPV == 32) ? 0xffffffffu
+                                    : (((1u << LPV) - 1u) << (lane & ~(unsigned)(LPV - 1)));
+#pragma unroll
+  for (int o = LPV / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(mask, v, o));
+  return v;
+}
+
+// One group of LPV = D/8 lanes per (token, head, K|V) vector.
+template <int MODE, int D>
+__global__ void __launch_bounds__(256) write_kernel(WriteArgs a) {
+  constexpr int LPV = D / 8;
+  const long long lane_id = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int sub = threadIdx.x % LPV;
+  const long long per_tensor = a.T * a.Hkv;
+  const long long n_vec = 2 * per_tensor;
+  const long long stride_vec = ((long long)gridDim.x * blockDim.x) / LPV;
+  for (long long vec = lane_id / LPV; vec < n_vec; vec += stride_vec) {
+    const int is_v = vec >= per_tensor;
+    const long long th = is_v ? vec - per_tensor : vec;
+    const long long t = th / a.Hkv;
+    const int h = (int)(th - t * a.Hkv);
+    const long long slot = a.slots[t];
+    if (slot < 0) continue;                                  // whole group agrees
+    if (slot >= a.num_blocks * a.bs) {
+      if (sub == 0 && !is_v && h == 0) atomicOr(a.err, ERR_BAD_INDEX);
+      continue;
+    }
+    const long long blk = slot / a.bs;
+    const int off = (int)(slot - blk * a.bs);
+    const long long cell = (blk * a.Hkv + h) * a.bs + off;
+    const uint16_t* src = (is_v ? a.v_new : a.k_new) + t * a.token_stride + (long long)h * D;
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src) + sub);
+    uint8_t* cache = is_v ? a.v_cache : a.k_cache;
+
+    if constexpr (MODE == BF16) {
+      reinterpret_cast<uint4*>(cache + cell * (2 * D))[sub] = raw;
+    } else {
+      float x[8];
+      x[0] = bf16_lo(raw.x); x[1] = bf16_hi(raw.x);
+      x[2] = bf16_lo(raw.y); x[3] = bf16_hi(raw.y);
+      x[4] = bf16_lo(raw.z); x[5] = bf16_hi(raw.z);
+      x[6] = bf16_lo(raw.w); x[7] = bf16_hi(raw.w);
+      float s;
+      if constexpr (MODE == FP8_PER_TENSOR) {
+        s = __ldg(is_v ? a.v_scale : a.k_scale);
+      } else if constexpr (MODE == FP8_PER_HEAD) {
+        s = __ldg((is_v ? a.v_scale : a.k_scale) + h);
+      } else {
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+        m = group_max<LPV>(m);
+        constexpr float qmax = (MODE == INT4_PER_TOKEN_HEAD) ? 7.0f : 448.0f;
+        s = (m == 0.f) ? 1.0f : __fdiv_rn(m, qmax);
+        if (sub == 0) (is_v ? a.v_cs : a.k_cs)[cell] = s;
+      }
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(x[i], s);
+      if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) packed |= int4_code(y[i]) << (4 * i);
+        reinterpret_cast<uint32_t*>(cache + cell * (D / 2))[sub] = packed;
+      } else {
+        uint2 o;
+        o.x = e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16);
+        o.y = e4m3x2(y[4], y[5]) | (e4m3x2(y[6], y[7]) << 16);
+        reinterpret_cast<uint2*>(cache + cell * D)[sub] = o;
+      }
+    }
+  }
+}
+
+template <int MODE>
+cudaError_t launch_mode(int D, const WriteArgs& a, cudaStream_t st) {
+  const long long lanes_needed = 2 * a.T * a.Hkv * (D / 8);
+  const int threads = 256;
+  long long blocks = (lanes_needed + threads - 1) / threads;
+  const long long cap = (long long)sm_count() * 8 * 16;     // enough waves, grid-stride beyond
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  switch (D) {
+    case 64: write_kernel<MODE, 64><<<(unsigned)blocks, threads, 0, st>>>(a); break;
+    case 128: write_kernel<MODE, 128><<<(unsigned)blocks, threads, 0, st>>>(a); break;
+    case 256: write_kernel<MODE, 256><<<(unsigned)blocks, threads, 0, st>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- calibration
+// amax per KV head over a [T][Hkv][D] bf16 sample.  Positive floats order like
+// their bit patterns, so an integer atomicMax on the bits is a float max.
+__global__ void calib_zero(unsigned* amax_bits, int Hkv) {
+  int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h < Hkv) amax_bits[h] = 0u;
+}
+
+// Grid: x over token chunks, y = KV head.  One atomic per block.
+__global__ void calib_amax(const uint16_t* x, long long T, int Hkv, int D, unsigned* amax_bits) {
+  const int h = blockIdx.y;
+  const long long n = T * D;                 // elements of head h
+  float m = 0.f;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long t = i / D, d = i - t * D;
+    m = fmaxf(m, fabsf(__uint_as_float((uint32_t)x[(t * Hkv + h) * D + d] << 16)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float wmax[32];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r = fmaxf(r, wmax[w]);
+    atomicMax(amax_bits + h, __float_as_uint(r));
+  }
+}
+
+__global__ void calib_finish(unsigned* amax_bits, int Hkv, float qmax) {
+  int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h < Hkv) {
+    const float m = __uint_as_float(amax_bits[h]);
+    reinterpret_cast<float*>(amax_bits)[h] = (m == 0.f) ? 1.0f : __fdiv_rn(m, qmax);
+  }
+}
+
+__global__ void e4m3_encode_kernel(const float* in, uint8_t* out, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    out[i] = (uint8_t)(e4m3x2(in[i], 0.f) & 0xFFu);
+}
+
+}  // namespace
+
+cudaError_t launch_cache_write(int mode, int D, const WriteArgs& a, cudaStream_t st) {
+  if (a.T == 0) return cudaSuccess;
+  switch (mode) {
+    case BF16: return launch_mode<BF16>(D, a, st);
+    case FP8_PER_TENSOR: return launch_mode<FP8_PER_TENSOR>(D, a, st);
+    case FP8_PER_HEAD: return launch_mode<FP8_PER_HEAD>(D, a, st);
+    case FP8_PER_TOKEN_HEAD: return launch_mode<FP8_PER_TOKEN_HEAD>(D, a, st);
+    case INT4_PER_TOKEN_HEAD: return launch_mode<INT4_PER_TOKEN_HEAD>(D, a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_calibrate(const uint16_t* x, long long T, int Hkv, int D, float qmax,
+                             float* out, cudaStream_t st) {
+  unsigned* bits = reinterpret_cast<unsigned*>(out);
+  const int tb = 256;
+  calib_zero<<<(Hkv + tb - 1) / tb, tb, 0, st>>>(bits, Hkv);
+  const long long n = T * D;
+  if (n > 0) {
+    long long blocks = (n + tb - 1) / tb;
+    if (blocks > 64) blocks = 64;
+    calib_amax<<<dim3((unsigned)blocks, (unsigned)Hkv), tb, 0, st>>>(x, T, Hkv, D, bits);
+  }
+  calib_finish<<<(Hkv + tb - 1) / tb, tb, 0, st>>>(bits, Hkv, qmax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, long long n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int tb = 256;
+  long long blocks = (n + tb - 1) / tb;
+  const long long cap = (long long)sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  e4m3_encode_kernel<<<(unsigned)blocks, tb, 0, st>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

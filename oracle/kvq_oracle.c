@@ -91,6 +91,12 @@ uint8_t orc_e4m3_encode(float y) {
   return (uint8_t)(sign | (uint32_t)(((e + 7) << 3) + (int)n - 8));
 }
 
+/* The encoder over an array (for exhaustive checks). */
+void orc_e4m3_encode_array(const float* y, uint8_t* out, long long n) {
+#pragma omp parallel for schedule(static)
+  for (long long i = 0; i < n; ++i) out[i] = orc_e4m3_encode(y[i]);
+}
+
 /* E4M3 code -> value (exact in double).  0x7F / 0xFF are NaN. */
 double orc_e4m3_decode(uint8_t c) {
   int s = c >> 7, E = (c >> 3) & 0xF, m = c & 7;

@@ -56,6 +56,8 @@ def lib():
             i32, i64, f32, f64 = ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_double
             L.orc_e4m3_encode.restype = ctypes.c_uint8
             L.orc_e4m3_encode.argtypes = [f32]
+            L.orc_e4m3_encode_array.restype = None
+            L.orc_e4m3_encode_array.argtypes = [P, P, i64]
             L.orc_e4m3_decode.restype = f64
             L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
             L.orc_int4_encode.restype = i32

@@ -1,0 +1,152 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, validates arguments on the host, and its capacity accounting matches
+the pages' formulas (oracle/accounting.py) and printed numbers."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+from oracle import accounting as acc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+GOLD = json.load(open(os.path.join(ROOT, "tests", "golden", "accounting.json")))
+
+kvq = pytest.importorskip("int4_quantized_paged_gb300.kvq",
+                          reason="libkvq.so not built (run __graft_entry__.build())")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 11
+    lib = ctypes.CDLL(kvq.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _ctx(modes, windows=None, Hq=32, Hkv=8, D=128, bs=16, nb=64):
+    return kvq.kvq_create(len(modes), Hq, Hkv, D, bs, nb, modes, windows)
+
+
+def test_create_validates_config():
+    with pytest.raises(kvq.KVQError, match="UNSUPPORTED"):
+        _ctx([3], D=96)
+    with pytest.raises(kvq.KVQError, match="UNSUPPORTED"):
+        _ctx([3], bs=24)
+    with pytest.raises(kvq.KVQError, match="INVALID_ARG"):
+        _ctx([3], Hq=30)
+    with pytest.raises(kvq.KVQError, match="INVALID_ARG"):
+        _ctx([7])
+    with pytest.raises(kvq.KVQError, match="INVALID_ARG"):
+        _ctx([3], windows=[-1])
+    with pytest.raises(kvq.KVQError, match="UNSUPPORTED"):
+        _ctx([3], Hq=96, Hkv=4)      # GQA ratio 24 not built
+
+
+def test_layer_buffer_sizes():
+    ctx = _ctx([0, 1, 2, 3, 4], nb=10)
+    cells = 10 * 8 * 16
+    assert kvq.kvq_layer_buffer_sizes(ctx, 0) == (cells * 256, 0)
+    assert kvq.kvq_layer_buffer_sizes(ctx, 1) == (cells * 128, 0)
+    assert kvq.kvq_layer_buffer_sizes(ctx, 2) == (cells * 128, 0)
+    assert kvq.kvq_layer_buffer_sizes(ctx, 3) == (cells * 128, cells * 4)
+    assert kvq.kvq_layer_buffer_sizes(ctx, 4) == (cells * 64, cells * 4)
+    with pytest.raises(kvq.KVQError):
+        kvq.kvq_layer_buffer_sizes(ctx, 5)
+
+
+def test_capacity_32_layer_example():
+    g = GOLD["gqa_32_layer"]
+    ctx = _ctx([3] * g["layers"], Hq=32, Hkv=g["kv_heads"], D=g["head_size"])
+    r = kvq.kvq_cache_bytes(ctx, g["context"])
+    assert r["payload_bytes_per_token"] == acc.payload_bytes_per_token(32, 8, 128, 1)
+    assert r["scale_bytes_per_token"] == acc.dynamic_scale_bytes_per_token(32, 8)
+    assert r["bytes_per_token"] / 1024 == g["total_kib_per_token"]
+    assert r["block_bytes"] / 1024 == g["block_kib"]
+    assert r["cache_bytes"] / 2 ** 30 == g["total_gib"]
+    assert r["bf16_cache_bytes"] / 2 ** 30 == g["bf16_gib"]
+
+
+def test_capacity_80_layer_static_metadata():
+    g = GOLD["fp8_80_layer_128k"]
+    for mode, key in ((1, "per_tensor_metadata_bytes"), (2, "static_per_head_metadata_bytes")):
+        ctx = _ctx([mode] * 80)
+        r = kvq.kvq_cache_bytes(ctx, g["context"])
+        assert r["static_scale_bytes"] == g[key]
+        assert r["cache_bytes"] - r["static_scale_bytes"] == g["fp8_kv_bytes"]
+    ctx = _ctx([3] * 80)
+    r = kvq.kvq_cache_bytes(ctx, g["context"])
+    assert r["cache_bytes"] / 2 ** 30 == g["fp8_plus_scales_gib"]
+
+
+def test_capacity_gpt_oss_skip_example():
+    g = GOLD["gpt_oss_20b_skip"]
+    wins = [128, 0] * 12
+    ref = acc.skip_accounting(g["context"], wins, [w > 0 for w in wins], 8, 64)
+    all_fp8 = kvq.kvq_cache_bytes(_ctx([1] * 24, wins, Hq=64, D=64), g["context"])
+    mixed = kvq.kvq_cache_bytes(_ctx([0, 1] * 12, wins, Hq=64, D=64), g["context"])
+    assert all_fp8["retained_positions"] == ref["A"]
+    assert all_fp8["cache_bytes"] - all_fp8["static_scale_bytes"] == ref["fp8_bytes"]
+    assert mixed["cache_bytes"] - mixed["static_scale_bytes"] == ref["mixed_bytes"]
+    assert all_fp8["bf16_cache_bytes"] == ref["bf16_bytes"]
+
+
+def test_write_rejects_bad_arguments_without_launching():
+    ctx = _ctx([3, 1])
+    ok = 0x10000000                       # never dereferenced: validation fails first
+    args = dict(k_new=ok, v_new=ok, slot_mapping=ok, k_cache=ok, v_cache=ok,
+                k_cache_scale=ok, v_cache_scale=ok)
+    L = kvq._lib
+
+    def write(layer=0, T=4, stride=0, **over):
+        a = dict(args, **over)
+        return L.kvq_cache_write(ctx, layer, a["k_new"], a["v_new"], stride, a["slot_mapping"],
+                                 T, a.get("k_scale"), a.get("v_scale"), a["k_cache"],
+                                 a["v_cache"], a["k_cache_scale"], a["v_cache_scale"], None)
+    assert write(T=0) == 0
+    assert write(T=-1) == 1
+    assert write(layer=2) == 1
+    assert write(k_new=None) == 1
+    assert write(k_cache_scale=None) == 1
+    assert write(layer=1) == 1                   # per-tensor needs k_scale / v_scale
+    assert write(k_new=ok + 8) == 3
+    assert write(k_cache=ok + 4) == 3
+    assert write(stride=8 * 128 + 4) == 3
+    assert write(stride=100) == 1
+
+
+def test_decode_plan_and_workspace_rules():
+    ctx = _ctx([3], Hq=64, Hkv=8, D=128)
+    s, ws = kvq.kvq_decode_plan(ctx, 0, 8, 131072)
+    assert s >= 1 and ws == (0 if s == 1 else 8 * 8 * s * 8 * 130 * 4)
+    s1, ws1 = kvq.kvq_decode_plan(ctx, 0, 8, 131072, num_splits=1)
+    assert (s1, ws1) == (1, 0)
+    s5, ws5 = kvq.kvq_decode_plan(ctx, 0, 8, 131072, num_splits=5)
+    assert (s5, ws5) == (5, 8 * 8 * 5 * 8 * 130 * 4)
+    ok = 0x10000000
+    L = kvq._lib
+    # too-small workspace is refused before launch
+    rc = L.kvq_decode_attention(ctx, 0, ok, ok, ok, None, None, ok, ok, ok, 8192, ok, 8, 131072,
+                                ok, 5, ok, ws5 - 1, None)
+    assert rc == 4
+    rc = L.kvq_decode_attention(ctx, 0, ok + 2, ok, ok, None, None, ok, ok, ok, 8192, ok, 8,
+                                131072, ok, 1, None, 0, None)
+    assert rc == 3
+    rc = L.kvq_decode_attention(ctx, 0, ok, ok, ok, None, None, None, ok, ok, 8192, ok, 8,
+                                131072, ok, 1, None, 0, None)
+    assert rc == 1
+    assert L.kvq_decode_attention(ctx, 0, ok, ok, ok, None, None, ok, ok, ok, 8192, ok, 0,
+                                  0, ok, 1, None, 0, None) == 0
+
+
+def test_status_strings():
+    for s in range(8):
+        assert kvq.kvq_status_string(s)

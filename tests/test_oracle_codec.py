@@ -110,3 +110,12 @@ def test_int4_round_half_even_and_clamp():
     ref = np.clip(np.round(ys), -7, 7).astype(int)   # numpy rounds half to even
     assert np.array_equal(got, ref)
     assert [orc.int4_encode(v) for v in (0.5, 1.5, 2.5, -2.5, 6.5, 7.4999)] == [0, 2, 2, -2, 6, 7]
+
+
+def test_array_encoder_matches_scalar_encoder():
+    rng = np.random.default_rng(11)
+    y = rng.integers(0, 2 ** 32, size=20000, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    out = np.empty(y.size, dtype=np.uint8)
+    orc.lib().orc_e4m3_encode_array(y.ctypes.data, out.ctypes.data, y.size)
+    ref = np.array([orc.e4m3_encode(v) for v in y], dtype=np.uint8)
+    assert np.array_equal(out, ref)
