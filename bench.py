@@ -243,16 +243,16 @@ def run_gpu(args):
     del k_all, v_all, slots_all
     q = wl.queries(w, dev)
     out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
-    splits, ws_bytes = kvq.kvq_decode_plan(ctx, 0, w.B, L, args.splits)
+    workers, ws_bytes = kvq.kvq_decode_plan(ctx, 0, w.B, L, args.workers)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    launches_per_step = 2 + (1 if splits > 1 else 0)
+    launches_per_step = 3          # write, decode, merge
 
     def step(qt=q, kn=k_new, vn=v_new, sl=slots_new, bt=pg.block_table, cl=pg.context_lens,
              o=out):
         kvq.kvq_cache_write(ctx, 0, kn, vn, sl, kc, vc, ks, vs, k_scale, v_scale)
         kvq.kvq_decode_attention(ctx, 0, qt, kc, vc, bt, cl, o, max_context=L, k_scale=k_scale,
                                  v_scale=v_scale, k_cache_scale=ks, v_cache_scale=vs,
-                                 num_splits=splits, workspace=ws)
+                                 num_workers=workers, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -276,7 +276,7 @@ def run_gpu(args):
         ev[i][1].record(stream)
         kvq.kvq_decode_attention(ctx, 0, q, kc, vc, pg.block_table, pg.context_lens, out,
                                  max_context=L, k_scale=k_scale, v_scale=v_scale,
-                                 k_cache_scale=ks, v_cache_scale=vs, num_splits=splits,
+                                 k_cache_scale=ks, v_cache_scale=vs, num_workers=workers,
                                  workspace=ws)
         ev[i][2].record(stream)
     t1.record(stream)
@@ -342,7 +342,7 @@ def run_gpu(args):
         "data": "synthetic (seeded N(0,1) x per-head log-uniform [0.5,32], 1% tokens x8)",
         "config": {"workload": "llama8b-like decode step: Hq=32 Hkv=8 D=128 block 16, "
                                "batch 64 x context 4096, 1 query/seq",
-                   "mode": args.mode, "num_splits": splits,
+                   "mode": args.mode, "num_workers": workers,
                    "l2": "inputs larger than L2: %.0f MB of cache read per step vs 129 MB L2"
                          % (dbytes / 1e6),
                    "parallelism": f"replicas x{world} (no exchange)"},
@@ -355,7 +355,7 @@ def run_gpu(args):
                        "bytes": wb_fill, "frac_of_peak": round(fill_gbs / peak, 4)},
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
-                     "kernel": "decode_kernel (+ split-K merge)",
+                     "kernel": "decode_kernel (+ log-sum-exp merge)",
                      "peak_source": f"{peak_src} hbm_gbs"},
         "e2e": {"value": round(all_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -471,7 +471,7 @@ def main(argv=None):
     ap.add_argument("--mode", default="fp8_per_token_head",
                     choices=["bf16", "fp8_per_tensor", "fp8_per_head", "fp8_per_token_head",
                              "int4_per_token_head"])
-    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--workers", type=int, default=0)
     ap.add_argument("--cpu-seqs", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

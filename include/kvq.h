@@ -141,12 +141,16 @@ kvq_status kvq_cache_write(const kvq_ctx* ctx, int layer, const void* k_new, con
 kvq_status kvq_calibrate_per_head(const kvq_ctx* ctx, const void* x, long long num_tokens,
                                   float qmax, float* scale_out, void* stream);
 
-/* Split-K plan for a decode call: the split count used when the caller
- * passes num_splits = 0 (from the batch, KV heads, longest context and the
- * device's SM count) and the workspace bytes a call with that split count
- * needs.  On input *num_splits may hold a requested count (>0) to size. */
+/* Work plan for a decode call.  The retained positions of all (sequence, KV
+ * head) items are cut into 16-position tiles and divided evenly among
+ * `num_workers` worker warps (split-K over the context, balanced whatever the
+ * context lengths); an item shared by several workers is merged by
+ * log-sum-exp.  On input *num_workers > 0 requests a count, 0 asks for the
+ * plan's choice (fill every SM, from the batch, KV heads, the longest
+ * context and the device); on output it holds the count and
+ * *workspace_bytes what a call with that count needs (0 for one worker). */
 kvq_status kvq_decode_plan(const kvq_ctx* ctx, int layer, int batch, int max_context,
-                           int* num_splits, size_t* workspace_bytes);
+                           int* num_workers, size_t* workspace_bytes);
 
 /* Paged decode attention, one query token per sequence.
  *
@@ -159,16 +163,17 @@ kvq_status kvq_decode_plan(const kvq_ctx* ctx, int layer, int batch, int max_con
  *   for a window W, else 0.  L = 0 gives a zero output row.
  * out: fp32 [batch][Hq][D] = sum_p softmax(softmax_scale <q, K_hat[p]>) V_hat[p]
  *   with K_hat = code x K scale, V_hat = code x V scale.
- * num_splits: >= 1 splits of each sequence's positions, merged by
- *   log-sum-exp; 0 = the plan's choice.  With more than one split the
- *   partials go to `workspace` (kvq_decode_plan gives its size).
+ * max_context: an upper bound of context_lens, used only by the plan.
+ * num_workers: worker warps (see kvq_decode_plan); 0 = the plan's choice.
+ *   With more than one worker, partials go to `workspace` (16-byte aligned,
+ *   kvq_decode_plan gives its size); its contents need no initialisation.
  * Scale pointers as for kvq_cache_write. */
 kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
                                 const void* k_cache, const void* v_cache, const float* k_scale,
                                 const float* v_scale, const float* k_cache_scale,
                                 const float* v_cache_scale, const int* block_table,
                                 int max_blocks_per_seq, const int* context_lens, int batch,
-                                int max_context, float* out, int num_splits, void* workspace,
+                                int max_context, float* out, int num_workers, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
 /* The device codec on its own: out[i] = E4M3 code of in[i] (RNE, saturating

@@ -8,7 +8,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/kvq.h"
+#include "kvq.h"
 #include "kvq_internal.h"
 
 struct kvq_ctx {
@@ -60,19 +60,17 @@ kvq_status check_layer(const kvq_ctx* ctx, int layer) {
 
 kvq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
-// Split count for a decode call: enough CTAs for about eight per SM, but at
-// least 8 tiles of 32 positions (256 positions) per split.
-int auto_splits(int batch, int Hkv, int max_positions) {
-  const long long pairs = (long long)batch * Hkv;
-  if (pairs <= 0 || max_positions <= 0) return 1;
-  const long long want = (long long)kvq::sm_count() * 8;
-  long long s = (want + pairs - 1) / pairs;
-  const long long tiles = (max_positions + 31) / 32;
-  const long long cap = tiles / 8 > 0 ? tiles / 8 : 1;
-  if (s > cap) s = cap;
-  if (s > 64) s = 64;
-  if (s < 1) s = 1;
-  return (int)s;
+// Worker warps for a decode call: enough to fill every SM at the kernel's
+// occupancy, but no more than one per 4 tiles (64 positions) of work, so a
+// worker always streams several tiles.
+int auto_workers(long long batch, int Hkv, int positions, int per_sm) {
+  const long long tiles = batch * Hkv * (((long long)positions + 15) / 16 + 1);
+  const long long full = (long long)kvq::sm_count() * (per_sm > 0 ? per_sm : 2) *
+                         kvq::decode_warps_per_cta();
+  long long w = tiles / 4;
+  if (w > full) w = full;
+  if (w < 1) w = 1;
+  return (int)w;
 }
 
 }  // namespace
@@ -212,20 +210,27 @@ kvq_status kvq_calibrate_per_head(const kvq_ctx* ctx, const void* x, long long n
 }
 
 kvq_status kvq_decode_plan(const kvq_ctx* ctx, int layer, int batch, int max_context,
-                           int* num_splits, size_t* workspace_bytes) {
+                           int* num_workers, size_t* workspace_bytes) {
   kvq_status st = check_layer(ctx, layer);
   if (st != KVQ_OK) return st;
-  if (!num_splits || batch < 0 || max_context < 0) return KVQ_ERR_INVALID_ARG;
+  if (!num_workers || batch < 0 || max_context < 0) return KVQ_ERR_INVALID_ARG;
   const kvq_config& c = ctx->cfg;
   const int W = ctx->window[layer];
-  const int positions = (W > 0 && W < max_context) ? W + 31 : max_context;
-  int s = *num_splits > 0 ? *num_splits : auto_splits(batch, c.num_kv_heads, positions);
-  *num_splits = s;
+  const int positions = (W > 0 && W < max_context) ? W + 15 : max_context;
+  const int G = c.num_q_heads / c.num_kv_heads;
+  int w = *num_workers > 0
+              ? *num_workers
+              : auto_workers(batch, c.num_kv_heads, positions,
+                             kvq::decode_ctas_per_sm(ctx->mode[layer], c.head_dim, G));
+  *num_workers = w;
   if (workspace_bytes) {
-    const int G = c.num_q_heads / c.num_kv_heads;
-    *workspace_bytes =
-        s <= 1 ? 0
-               : (size_t)batch * c.num_kv_heads * s * G * (c.head_dim + 2) * sizeof(float);
+    // one partial slot per (sequence, KV head) item plus one per worker, and
+    // the items' offsets in the tile list
+    const size_t items = (size_t)batch * c.num_kv_heads;
+    const size_t slots = items + (size_t)w;
+    *workspace_bytes = w <= 1 ? 0
+                              : slots * G * (c.head_dim + 2) * sizeof(float) +
+                                    (items + 1) * sizeof(long long);
   }
   return KVQ_OK;
 }
@@ -235,11 +240,11 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
                                 const float* v_scale, const float* k_cache_scale,
                                 const float* v_cache_scale, const int* block_table,
                                 int max_blocks_per_seq, const int* context_lens, int batch,
-                                int max_context, float* out, int num_splits, void* workspace,
+                                int max_context, float* out, int num_workers, void* workspace,
                                 size_t workspace_bytes, void* stream) {
   kvq_status st = check_layer(ctx, layer);
   if (st != KVQ_OK) return st;
-  if (batch < 0 || max_context < 0 || num_splits < 0 || max_blocks_per_seq < 0)
+  if (batch < 0 || max_context < 0 || num_workers < 0 || max_blocks_per_seq < 0)
     return KVQ_ERR_INVALID_ARG;
   if (batch == 0) return KVQ_OK;
   const kvq_config& c = ctx->cfg;
@@ -255,13 +260,13 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
     if (!k_cache_scale || !v_cache_scale) return KVQ_ERR_INVALID_ARG;
     if (!aligned4(k_cache_scale) || !aligned4(v_cache_scale)) return KVQ_ERR_ALIGNMENT;
   }
-  int splits = num_splits;
+  int workers = num_workers;
   size_t need = 0;
-  st = kvq_decode_plan(ctx, layer, batch, max_context, &splits, &need);
+  st = kvq_decode_plan(ctx, layer, batch, max_context, &workers, &need);
   if (st != KVQ_OK) return st;
-  if (splits > 1 && (!workspace || workspace_bytes < need)) return KVQ_ERR_WORKSPACE;
-  if (splits > 1 && !aligned16(workspace)) return KVQ_ERR_ALIGNMENT;
-  if (splits > 65535) return KVQ_ERR_INVALID_ARG;
+  if (workers > 1 && (!workspace || workspace_bytes < need)) return KVQ_ERR_WORKSPACE;
+  if (workers > 1 && !aligned16(workspace)) return KVQ_ERR_ALIGNMENT;
+  if ((long long)workers > 4LL * 65535 * 64) return KVQ_ERR_INVALID_ARG;
   unsigned* err = kvq::error_word();
   if (!err) return KVQ_ERR_CUDA;
   const int G = c.num_q_heads / c.num_kv_heads;
@@ -277,9 +282,11 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
   a.context_lens = context_lens;
   a.out = out;
   float* ws = static_cast<float*>(workspace);
-  const size_t n_part = (size_t)batch * c.num_kv_heads * splits * G;
-  a.ws_o = splits > 1 ? ws : nullptr;
-  a.ws_ml = splits > 1 ? ws + n_part * c.head_dim : nullptr;
+  const size_t n_part = ((size_t)batch * c.num_kv_heads + (size_t)workers) * G;
+  a.ws_o = workers > 1 ? ws : nullptr;
+  a.ws_ml = workers > 1 ? ws + n_part * c.head_dim : nullptr;
+  a.item_tiles = workers > 1 ? reinterpret_cast<long long*>(ws + n_part * (c.head_dim + 2))
+                             : nullptr;
   a.err = err;
   a.B = batch;
   a.Hq = c.num_q_heads;
@@ -287,7 +294,7 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
   a.bs = c.block_size;
   a.max_blocks = max_blocks_per_seq;
   a.window = ctx->window[layer];
-  a.splits = splits;
+  a.workers = workers;
   a.num_blocks = c.num_blocks;
   a.qk_scale = ctx->softmax_scale * 1.4426950408889634f;
   return cuda_status(

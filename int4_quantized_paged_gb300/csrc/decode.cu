@@ -1,22 +1,48 @@
-// Paged GQA decode attention over the quantized cache, with split-K over the
-// context and a log-sum-exp merge.
+// Paged GQA decode attention over the quantized cache.
 //
 // What it computes: for each sequence b and query head hq, the softmax over
 // retained positions p in [lo, L) of softmax_scale * <q, K_hat[p]> weights
-// V_hat[p]; K_hat = code * K scale, V_hat = code * V scale.  The K scale is
-// applied to the dot product of q with the raw codes and the V scale to the
-// softmax weight, so codes are never rescaled element by element.
-// Scale layouts: "Per-tensor vs per-head FP8 KV cache scales"; windows and
-// BF16 (skipped) layers: "FP8 KV cache layer skipping vs per-head scales",
-// sections "FP8 KV cache layer skipping vs per-head scales" and "Layer
-// skipping follows retained-token footprint".
+// V_hat[p]; K_hat = code * K scale, V_hat = code * V scale.  The K scale
+// multiplies the dot product of q with the raw codes and the V scale the
+// softmax weight, so codes are never rescaled element by element.  Scale
+// layouts: "Per-tensor vs per-head FP8 KV cache scales"; packed INT4:
+// "Per-token-head KV cache scale overhead", section "INT4 makes the metadata
+// fraction larger"; windows and BF16 (skipped) layers: "FP8 KV cache layer
+// skipping vs per-head scales", sections "FP8 KV cache layer skipping vs
+// per-head scales" and "Layer skipping follows retained-token footprint".
 //
-// Decomposition: one CTA of 4 warps per (sequence, KV head, split).  The
-// split's positions are cut into 32-position tiles; warp w takes tiles w,
-// w+4, ...  In a tile, lane i owns position tile*32+i for the QK products of
-// all G query heads of the group (q lives in shared memory, pre-multiplied by
-// softmax_scale*log2(e)), the online softmax runs in log2 units, and the PV
-// update spreads the tile's V rows over the lanes, 8 elements per lane.
+// Work decomposition (split-K over the context, balanced over warps):
+//  * A sequence's retained positions are cut into 16-position tiles (a tile
+//    never straddles a page: block_size is a multiple of 16).  All tiles of
+//    all (sequence, KV head) items, in that order, form one list of T tiles.
+//    Worker warp w takes tiles [w T / W, (w+1) T / W): every warp gets the
+//    same number of tiles whatever the context lengths, and a warp's share
+//    runs across item boundaries.  For each item segment it covers, a warp
+//    either writes the final output (it covered the whole item) or a partial
+//    (running max m, sum l, unnormalised O) that a merge kernel combines by
+//    log-sum-exp.  Warps never wait on one another.
+//  * Each warp streams its tiles through an NS-stage ring in shared memory
+//    with TMA: a 2-D tensor copy each for the K and V code tile (128-byte
+//    rows, 128B swizzle so the fragment loads below hit no bank conflicts)
+//    and, for dynamic scales, a 64-byte bulk copy each of the tile's K and V
+//    scales, completing on the stage's mbarrier.  The copies of the next
+//    NS-1 tiles (of this or the next item) are in flight while one tile is
+//    computed.  Every wait is bounded: a wait that runs out sets the TIMEOUT
+//    bit of the device error word, drains the warp's copies and stops.
+//  * QK on tensor cores: S^T[16 positions x 8 columns] = K_tile . Q^T with
+//    mma.m16n8k16, fp32 accumulate.  E4M3 and INT4 codes convert exactly to
+//    f16; q (bf16) times a power of two converts exactly to f16.  Columns
+//    are the G query heads of the KV head.
+//  * Online softmax in log2 units on the fragments (running max over the raw
+//    scores).  The weights that meet V are P' = p * v_scale * 2^k, with k a
+//    power-of-two range factor that keeps P' below 2^14, so both f16 terms of
+//    its split stay normal numbers.
+//  * PV on tensor cores with d as the M dimension: O^T[d x cols] += V^T P'.
+//    P' is split into two f16 terms (hi + lo, about 22 bits; three bf16
+//    terms for BF16 layers) so the weighted sum keeps fp32-class accuracy;
+//    for G*terms <= 8 all terms share one 8-column tile.  The P' fragment
+//    comes from the S^T fragment by movmatrix (in-register 8x8 transpose).
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -26,263 +52,1075 @@
 namespace kvq {
 namespace {
 
-constexpr int WARPS = 4;
-constexpr int TILE = 32;
+constexpr int WARPS = 4;         // worker warps per CTA (independent)
+#ifndef KVQ_WAIT_HINT_NS
+#define KVQ_WAIT_HINT_NS 0     // suspend-time hint of one mbarrier try (0: none)
+#endif
+#ifndef KVQ_TILES_PER_ITER
+#define KVQ_TILES_PER_ITER 1
+#endif
+constexpr int PAIR = KVQ_TILES_PER_ITER;   // 16-position tiles per loop iteration
+constexpr int TILE = 16;         // positions per tile
+constexpr long long SPIN_LIMIT_CYCLES = 4000000000LL;   // about 2 s at 2 GHz
 
+// ------------------------------------------------------------------ PTX
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
-// Two E4M3 codes (low byte first) -> two floats; the conversion is exact.
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
-  uint32_t h2;
-  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(two));
-  const unsigned short lo = (unsigned short)(h2 & 0xFFFFu), hi = (unsigned short)(h2 >> 16);
-  float2 r;
-  asm("cvt.f32.f16 %0, %1;" : "=f"(r.x) : "h"(lo));
-  asm("cvt.f32.f16 %0, %1;" : "=f"(r.y) : "h"(hi));
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// One try.  With a suspend-time hint (ns) the thread may sleep until the
+// phase completes instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+#if KVQ_WAIT_HINT_NS > 0
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)KVQ_WAIT_HINT_NS)
+      : "memory");
+#else
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+#endif
+  return ok != 0;
+}
+
+// Bounded wait; returns false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > SPIN_LIMIT_CYCLES) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_tile_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Four E4M3 codes (one word) -> two f16x2: bytes 0,1 -> lo; bytes 2,3 -> hi.
+// The conversion is exact.
+__device__ __forceinline__ void e4m3x4_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.rn.f16x2.e4m3x2 %0, a; cvt.rn.f16x2.e4m3x2 %1, b; }"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Two nibble values placed at bits 0-3 and 16-19, offset binary (n ^ 8) ->
+// f16x2 of the signed values (exact): f16(1024 + m) - 1032.
+__device__ __forceinline__ uint32_t nib2_f16x2(uint32_t x) {
+  uint32_t h = (x & 0x000F000Fu) | 0x64006400u, r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64086408u));
   return r;
 }
 
-// 8 row elements starting at element 8*c of a cached row, as floats (codes,
-// not yet scaled).
-template <int MODE, int D>
-__device__ __forceinline__ void load8(const uint8_t* row, int c, float v[8]) {
-  if constexpr (MODE == BF16) {
-    const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * c);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = __uint_as_float(ws[i] << 16);
-      v[2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
-    }
-  } else if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(row + 4 * c);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = (float)(((int)(w << (28 - 4 * i))) >> 28);
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t h2) {
+  float f;
+  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %1; cvt.f32.f16 %0, a; }" : "=f"(f) : "r"(h2));
+  return f;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t h2) { return __uint_as_float(h2 << 16); }
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
+template <bool BF>
+__device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32_t b0,
+                                         uint32_t b1) {
+  if constexpr (BF) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   } else {
-    const uint2 w = *reinterpret_cast<const uint2*>(row + 8 * c);
-    float2 a = e4m3x2_to_float2(w.x & 0xFFFFu), b = e4m3x2_to_float2(w.x >> 16);
-    float2 d = e4m3x2_to_float2(w.y & 0xFFFFu), e = e4m3x2_to_float2(w.y >> 16);
-    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
-    v[4] = d.x; v[5] = d.y; v[6] = e.x; v[7] = e.y;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
 }
 
+// ------------------------------------------------------------------ layout
 template <int MODE>
 constexpr int row_bytes(int D) {
   return MODE == BF16 ? 2 * D : (MODE == INT4_PER_TOKEN_HEAD ? D / 2 : D);
 }
 
-template <int MODE, int D, int G>
-__global__ void __launch_bounds__(WARPS * 32) decode_kernel(DecodeArgs a) {
+// Shared-memory byte offset of logical byte `o` of a tile written by a TMA
+// copy with 128-byte rows and 128B swizzle (buffer 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz(uint32_t o) {
+  return o ^ (((o >> 7) & 7u) << 4);
+}
+
+template <int N>
+__device__ __forceinline__ void lds(uint32_t (&r)[N], const uint8_t* base, uint32_t o) {
+  static_assert(N == 1 || N == 2 || N == 4, "");
+  const uint8_t* p = base + swz(o);
+  if constexpr (N == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    r[0] = v.x; r[1] = v.y; r[2] = v.z; r[3] = v.w;
+  } else if constexpr (N == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    r[0] = v.x; r[1] = v.y;
+  } else {
+    r[0] = *reinterpret_cast<const uint32_t*>(p);
+  }
+}
+
+// d index of QK k-slot j (0: 2t, 1: 2t+1, 2: 2t+8, 3: 2t+9) at k-step s for
+// lane column t: the order the QK A-fragment loader produces.
+template <int MODE, int D>
+__device__ __forceinline__ int qk_d(int t, int s, int j) {
+  if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
+    const int base = t * (D / 4) + 8 * (s >> 1) + 2 * (s & 1);
+    const int off[4] = {0, 4, 1, 5};
+    return base + off[j];
+  } else {
+    return t * (D / 4) + 4 * s + j;
+  }
+}
+
+// Term k of the split of a weight x into f16 (hi, lo) or bf16 (hi, mid, lo)
+// parts whose sum reproduces x to about 22 (f16) or 24 (bf16) bits.
+template <bool BF>
+__device__ __forceinline__ float split_term(float x, int k) {
+  if constexpr (BF) {
+    const float h = bf16_lo(pack_bf16x2(x, 0.f));
+    const float r = x - h;
+    const float m = bf16_lo(pack_bf16x2(r, 0.f));
+    return k == 0 ? h : (k == 1 ? m : r - m);
+  } else {
+    const float h = f16_lo(pack_f16x2(x, 0.f));
+    return k == 0 ? h : x - h;
+  }
+}
+
+// SEG bytes of a token row segment from a swizzled tile into 32-bit words;
+// zeros when the token is masked (its bytes may be anything).
+template <int SEG>
+__device__ __forceinline__ void load_seg(uint32_t* w, const uint8_t* tile, uint32_t off, bool ok) {
+  if constexpr (SEG >= 16) {
+#pragma unroll
+    for (int h = 0; h < SEG / 16; ++h) {
+      uint32_t r[4];
+      lds<4>(r, tile, off + 16 * h);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) w[4 * h + e] = ok ? r[e] : 0u;
+    }
+  } else if constexpr (SEG == 8) {
+    uint32_t r[2];
+    lds<2>(r, tile, off);
+    w[0] = ok ? r[0] : 0u;
+    w[1] = ok ? r[1] : 0u;
+  } else {
+    uint32_t r[1];
+    lds<1>(r, tile, off);
+    w[0] = ok ? r[0] : 0u;
+  }
+}
+
+// 2^e for e in [-126, 127] (exact, from the exponent bits); 0 below.
+__device__ __forceinline__ float pow2i(int e) {
+  return e < -126 ? 0.f : __uint_as_float((uint32_t)(e + 127) << 23);
+}
+
+// Unbiased exponent of a positive normal float.
+__device__ __forceinline__ int f32_exp(float x) {
+  return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
+}
+
+// QK of one 16-position sub-tile: sacc (rows lg, lg+8; columns 2lt, 2lt+1)
+// += K_tile . Q^T.  The lane reads its D/4-element segment of rows lg, lg+8.
+template <int MODE, int D>
+__device__ __forceinline__ void qk_tile(float sacc[4], const uint8_t* kt, int lg, int lt,
+                                        const uint32_t (*qf)[2]) {
   constexpr int RB = row_bytes<MODE>(D);
-  constexpr int LPR = D / 8;            // lanes per row in the PV phase
-  constexpr int RPI = 32 / LPR;         // rows per pass in the PV phase
-  constexpr bool DYN = (MODE == FP8_PER_TOKEN_HEAD || MODE == INT4_PER_TOKEN_HEAD);
-
-  __shared__ __align__(16) float q_s[G][D];
-  __shared__ float p_s[WARPS][TILE][G];
-  __shared__ long long row_s[WARPS][TILE];      // cell index of each tile row, -1 = none
-  __shared__ float m_s[WARPS][G], l_s[WARPS][G];
-  __shared__ __align__(16) float o_s[WARPS][G][D];
-
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int j = i / D, d = i - j * D;
-    const uint16_t qb = a.q[((long long)b * a.Hq + g * G + j) * D + d];
-    q_s[j][d] = __uint_as_float((uint32_t)qb << 16) * a.qk_scale;
-  }
-  __syncthreads();
-
-  int L = a.context_lens[b];
-  if (L < 0) {
-    if (threadIdx.x == 0 && split == 0 && g == 0) atomicOr(a.err, ERR_BAD_INDEX);
-    L = 0;
-  }
-  const int lo = (a.window > 0 && L > a.window) ? L - a.window : 0;
-  const int t0 = lo / TILE, t1 = (L + TILE - 1) / TILE;
-  const int n_tiles = t1 - t0;
-  const int tps = (n_tiles + a.splits - 1) / a.splits;
-  const int my_t0 = t0 + split * tps;
-  const int my_t1 = min(t1, my_t0 + tps);
-
-  float ks_static = 1.f, vs_static = 1.f;
-  if constexpr (MODE == FP8_PER_TENSOR) { ks_static = a.k_scale[0]; vs_static = a.v_scale[0]; }
-  if constexpr (MODE == FP8_PER_HEAD) { ks_static = a.k_scale[g]; vs_static = a.v_scale[g]; }
-
-  float m[G], l[G], o[G][8];
+  constexpr int KSTEPS = D / 16;
+  const int r0 = lg, r1 = lg + 8;
+  if constexpr (MODE == BF16) {
 #pragma unroll
-  for (int j = 0; j < G; ++j) {
-    m[j] = -INFINITY;
-    l[j] = 0.f;
+    for (int s4 = 0; s4 < KSTEPS; s4 += 2) {
+      uint32_t w0[4], w1[4];
+      lds<4>(w0, kt, r0 * RB + lt * (D / 2) + 8 * s4);
+      lds<4>(w1, kt, r1 * RB + lt * (D / 2) + 8 * s4);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[j][e] = 0.f;
-  }
-
-  const int pr = lane / LPR, pc = lane % LPR;   // PV-phase row group and column chunk
-  const int* bt = a.block_table + (long long)b * a.max_blocks;
-
-  for (int tile = my_t0 + warp; tile < my_t1; tile += WARPS) {
-    // ---- QK: lane owns one position
-    const int pos = tile * TILE + lane;
-    long long cell = -1;
-    if (pos >= lo && pos < L) {
-      const int blk = bt[pos / a.bs];
-      if (blk >= 0 && blk < a.num_blocks) {
-        cell = ((long long)blk * a.Hkv + g) * a.bs + (pos % a.bs);
-      } else {
-        atomicOr(a.err, ERR_BAD_INDEX);
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t af[4] = {w0[2 * u], w1[2 * u], w0[2 * u + 1], w1[2 * u + 1]};
+        mma16816<true>(sacc, af, qf[s4 + u][0], qf[s4 + u][1]);
       }
     }
-    float s[G];
+  } else if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
+    constexpr int SEGB = D / 8;          // bytes of the lane segment; a word = two k-steps
+    constexpr int NW = SEGB / 4;
+    uint32_t w0[NW], w1[NW];
+    load_seg<SEGB>(w0, kt, r0 * RB + lt * SEGB, true);
+    load_seg<SEGB>(w1, kt, r1 * RB + lt * SEGB, true);
 #pragma unroll
-    for (int j = 0; j < G; ++j) s[j] = 0.f;
-    float vsc = 0.f;
-    if (cell >= 0) {
-      const uint8_t* krow = a.k_cache + cell * RB;
-#pragma unroll 4
-      for (int c = 0; c < D / 8; ++c) {
-        float kv[8];
-        load8<MODE, D>(krow, c, kv);
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          const float4 qa = *reinterpret_cast<const float4*>(&q_s[j][8 * c]);
-          const float4 qb = *reinterpret_cast<const float4*>(&q_s[j][8 * c + 4]);
-          s[j] += qa.x * kv[0] + qa.y * kv[1] + qa.z * kv[2] + qa.w * kv[3] +
-                  qb.x * kv[4] + qb.y * kv[5] + qb.z * kv[6] + qb.w * kv[7];
-        }
-      }
-      const float ksc = DYN ? a.k_cs[cell] : ks_static;
-      vsc = DYN ? a.v_cs[cell] : vs_static;
-#pragma unroll
-      for (int j = 0; j < G; ++j) s[j] *= ksc;
-    } else {
-#pragma unroll
-      for (int j = 0; j < G; ++j) s[j] = -INFINITY;
+    for (int s = 0; s < KSTEPS; ++s) {
+      const int sh = 8 * (s & 1);
+      const uint32_t x0 = w0[s >> 1] ^ 0x88888888u, x1 = w1[s >> 1] ^ 0x88888888u;
+      const uint32_t af[4] = {nib2_f16x2(x0 >> sh), nib2_f16x2(x1 >> sh),
+                              nib2_f16x2(x0 >> (sh + 4)), nib2_f16x2(x1 >> (sh + 4))};
+      mma16816<false>(sacc, af, qf[s][0], qf[s][1]);
     }
-    // ---- online softmax (log2 units)
-    float alpha[G];
+  } else {
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
-      float mt = s[j];
+    for (int s4 = 0; s4 < KSTEPS; s4 += 4) {
+      uint32_t w0[4], w1[4];
+      lds<4>(w0, kt, r0 * RB + lt * (D / 4) + 4 * s4);
+      lds<4>(w1, kt, r1 * RB + lt * (D / 4) + 4 * s4);
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-      const float mn = fmaxf(m[j], mt);
-      if (mn == -INFINITY) {
-        alpha[j] = 1.f;
-        p_s[warp][lane][j] = 0.f;
-      } else {
-        alpha[j] = ex2(m[j] - mn);           // m = -inf -> 0
-        const float p = (cell >= 0) ? ex2(s[j] - mn) : 0.f;
-        l[j] = l[j] * alpha[j] + p;          // per-lane partial sum
-        p_s[warp][lane][j] = p * vsc;
+      for (int u = 0; u < 4; ++u) {
+        uint32_t af[4];
+        e4m3x4_f16(w0[u], af[0], af[2]);
+        e4m3x4_f16(w1[u], af[1], af[3]);
+        mma16816<false>(sacc, af, qf[s4 + u][0], qf[s4 + u][1]);
       }
-      m[j] = mn;
-    }
-    row_s[warp][lane] = cell;
-    __syncwarp();
-    // ---- PV: lane group pr walks rows pr, pr+RPI, ...; column chunk pc
-#pragma unroll
-    for (int j = 0; j < G; ++j)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[j][e] *= alpha[j];
-    for (int r = pr; r < TILE; r += RPI) {
-      const long long vc = row_s[warp][r];
-      if (vc < 0) continue;
-      float vv[8];
-      load8<MODE, D>(a.v_cache + vc * RB, pc, vv);
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        const float p = p_s[warp][r][j];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[j][e] += p * vv[e];
-      }
-    }
-    __syncwarp();
-  }
-
-  // ---- reduce inside the warp: l over lanes, o over the RPI row groups
-#pragma unroll
-  for (int j = 0; j < G; ++j) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
-#pragma unroll
-    for (int off = LPR; off < 32; off <<= 1)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[j][e] += __shfl_xor_sync(0xffffffffu, o[j][e], off);
-  }
-  if (lane < LPR) {
-#pragma unroll
-    for (int j = 0; j < G; ++j)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o_s[warp][j][8 * pc + e] = o[j][e];
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int j = 0; j < G; ++j) { m_s[warp][j] = m[j]; l_s[warp][j] = l[j]; }
-  }
-  __syncthreads();
-
-  // ---- combine the warps, then write the output or the split's partial
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int j = i / D, d = i - j * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, m_s[w][j]);
-    float acc = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < WARPS; ++w) {
-        const float f = ex2(m_s[w][j] - M);
-        acc += f * o_s[w][j][d];
-        den += f * l_s[w][j];
-      }
-    }
-    const long long head = (long long)b * a.Hq + g * G + j;
-    if (a.splits == 1) {
-      a.out[head * D + d] = den > 0.f ? acc / den : 0.f;
-    } else {
-      const long long part = (((long long)b * a.Hkv + g) * a.splits + split) * G + j;
-      a.ws_o[part * D + d] = acc;
-      if (d == 0) { a.ws_ml[2 * part] = M; a.ws_ml[2 * part + 1] = den; }
     }
   }
 }
 
-// Log-sum-exp merge of the splits: one CTA of D threads per (sequence, KV head).
-template <int D, int G>
-__global__ void __launch_bounds__(D) merge_kernel(DecodeArgs a) {
-  const int g = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-  const long long base = ((long long)b * a.Hkv + g) * a.splits;
-  for (int j = 0; j < G; ++j) {
-    float M = -INFINITY;
-    for (int s = 0; s < a.splits; ++s) M = fmaxf(M, a.ws_ml[2 * ((base + s) * G + j)]);
-    float acc = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < a.splits; ++s) {
-        const long long part = (base + s) * G + j;
-        const float f = ex2(a.ws_ml[2 * part] - M);
-        acc += f * a.ws_o[part * D + d];
-        den += f * a.ws_ml[2 * part + 1];
+// PV of one 16-position sub-tile: acc[n][i] (rows d, columns) += V^T . P'.
+// The lane reads its d-segment of positions 2lt, 2lt+1, 2lt+8, 2lt+9; with
+// WHOLE false, positions outside [lo, L) are zeroed (their bytes may be
+// anything).
+template <int MODE, int D, int NT, bool WHOLE>
+__device__ __forceinline__ void pv_tile(float (*acc)[D / 16][4], const uint8_t* vt, int lg,
+                                        int lt, const uint32_t (*pb)[2], int pos0, int lo, int L) {
+  constexpr int RB = row_bytes<MODE>(D);
+  constexpr int SEG = (MODE == BF16) ? D / 4 : (MODE == INT4_PER_TOKEN_HEAD ? D / 16 : D / 8);
+  constexpr int SW = SEG / 4;
+  constexpr bool BF = (MODE == BF16);
+  const int ta = 2 * lt, tb = 2 * lt + 1, tc = 2 * lt + 8, td = 2 * lt + 9;
+  bool va = true, vb = true, vc = true, vd = true;
+  if constexpr (!WHOLE) {
+    va = pos0 + ta >= lo && pos0 + ta < L;
+    vb = pos0 + tb >= lo && pos0 + tb < L;
+    vc = pos0 + tc >= lo && pos0 + tc < L;
+    vd = pos0 + td >= lo && pos0 + td < L;
+  }
+  uint32_t wa[SW], wb[SW], wc[SW], wd[SW];
+  const int seg0 = lg * SEG;
+  load_seg<SEG>(wa, vt, ta * RB + seg0, va);
+  load_seg<SEG>(wb, vt, tb * RB + seg0, vb);
+  load_seg<SEG>(wc, vt, tc * RB + seg0, vc);
+  load_seg<SEG>(wd, vt, td * RB + seg0, vd);
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) {
+    uint32_t af[4];
+    if constexpr (MODE == BF16) {
+      // elements 2i and 2i+1 of each position's segment = word i
+      af[0] = __byte_perm(wa[i], wb[i], 0x5410);
+      af[1] = __byte_perm(wa[i], wb[i], 0x7632);
+      af[2] = __byte_perm(wc[i], wd[i], 0x5410);
+      af[3] = __byte_perm(wc[i], wd[i], 0x7632);
+    } else if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
+      // byte i of the segment: low nibble = d 2i, high nibble = d 2i+1
+      const int wi = i >> 2, k = i & 3;
+      const uint32_t sel = (uint32_t)(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
+      const uint32_t x = __byte_perm(wa[wi], wb[wi], sel) ^ 0x00880088u;
+      const uint32_t y = __byte_perm(wc[wi], wd[wi], sel) ^ 0x00880088u;
+      af[0] = nib2_f16x2(x);
+      af[1] = nib2_f16x2(x >> 4);
+      af[2] = nib2_f16x2(y);
+      af[3] = nib2_f16x2(y >> 4);
+    } else {
+      // bytes 2i, 2i+1 of each position's segment
+      const int wi = i >> 1;
+      const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+      e4m3x4_f16(__byte_perm(wa[wi], wb[wi], sel), af[0], af[1]);
+      e4m3x4_f16(__byte_perm(wc[wi], wd[wi], sel), af[2], af[3]);
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) mma16816<BF>(acc[n][i], af, pb[n][0], pb[n][1]);
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int MODE, int D>
+struct Cfg {
+  static constexpr int RB = row_bytes<MODE>(D);
+  static constexpr int TB = TILE * RB;                       // tile bytes
+  static constexpr int TBP = (TB + 1023) / 1024 * 1024;      // padded to 1024
+  static constexpr bool DYN = (MODE == FP8_PER_TOKEN_HEAD || MODE == INT4_PER_TOKEN_HEAD);
+  static constexpr bool BF = (MODE == BF16);
+  static constexpr int STAGE = 2 * TBP;                      // K + V code tiles
+  static constexpr int SCALES = DYN ? 128 : 0;               // K + V scales per stage
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int MTILES = D / 16;
+  // ring stages per warp: PAIR tiles per iteration plus at least one in
+  // flight; about 13 KB (one tile per iteration) or 18 KB (two) per warp
+  static constexpr int NS0 = (PAIR == 1 ? 13312 : 18432) / STAGE;
+  static constexpr int NSMIN = PAIR + 1;
+#ifdef KVQ_NS
+  static constexpr int NS = KVQ_NS < NSMIN ? NSMIN : KVQ_NS;
+#else
+  static constexpr int NS = NS0 < NSMIN ? NSMIN : (NS0 > 6 ? 6 : NS0);
+#endif
+};
+
+// Shared memory: the warps' rings first (1024-aligned stages for the
+// swizzled copies), then per warp its scale slots, q staging and barriers.
+template <int MODE, int D, int G>
+struct Layout {
+  using C = Cfg<MODE, D>;
+  static constexpr int ring = C::NS * C::STAGE;
+  static constexpr int scales = C::NS * C::SCALES;
+  static constexpr int q = G * D * 2;
+  static constexpr int bars = C::NS * 8;
+  static constexpr int aux = (scales + q + bars + 127) / 128 * 128;
+  static constexpr int total = WARPS * (ring + aux) + 1024;   // + alignment slack
+};
+
+// Position of one warp's cursor in the tile list.
+struct Cursor {
+  int b, g, k;      // sequence, KV head, tile within the item
+  int n, t0;        // tiles of the item, first tile index (position / 16)
+};
+
+__device__ __forceinline__ int seq_tiles(const DecodeArgs& a, int b, int* t0) {
+  int L = a.context_lens[b];
+  if (L < 0) L = 0;
+  const int lo = (a.window > 0 && L > a.window) ? L - a.window : 0;
+  *t0 = lo / TILE;
+  return L > 0 ? (L + TILE - 1) / TILE - lo / TILE : 0;
+}
+
+// Total tiles T (all lanes get it) and, if `find` >= 0, the cursor at tile
+// `find`.  Sequences are scanned 32 at a time with a warp prefix sum.
+__device__ long long scan_tiles(const DecodeArgs& a, long long find, Cursor* cur, int lane) {
+  long long base = 0;             // tiles before the current chunk of sequences
+  bool found = false;
+  for (int b0 = 0; b0 < a.B; b0 += 32) {
+    const int b = b0 + lane;
+    int t0 = 0, n = 0;
+    if (b < a.B) {
+      if (a.context_lens[b] < 0) atomicOr(a.err, ERR_BAD_INDEX);
+      n = seq_tiles(a, b, &t0);
+    }
+    long long incl = (long long)n * a.Hkv;       // inclusive prefix within the chunk
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const long long excl = incl - (long long)n * a.Hkv;
+    if (!found && find >= 0) {
+      const bool here = b < a.B && n > 0 && find >= base + excl && find < base + incl;
+      const unsigned m = __ballot_sync(0xffffffffu, here);
+      if (m) {
+        const int src = __ffs(m) - 1;
+        const long long off = __shfl_sync(0xffffffffu, find - base - excl, src);
+        const int nn = __shfl_sync(0xffffffffu, n, src);
+        cur->b = b0 + src;
+        cur->n = nn;
+        cur->t0 = __shfl_sync(0xffffffffu, t0, src);
+        cur->g = (int)(off / nn);
+        cur->k = (int)(off % nn);
+        found = true;
       }
     }
-    a.out[((long long)b * a.Hq + g * G + j) * D + d] = den > 0.f ? acc / den : 0.f;
+    base += __shfl_sync(0xffffffffu, incl, 31);
   }
+  return base;
+}
+
+// Worker 0: item tile offsets P_i (i = b*Hkv + g; P_{B*Hkv} = T) for the
+// merge, and zeros for the output of every sequence with no retained position.
+template <int G, int D>
+__device__ void publish_items(const DecodeArgs& a, int lane) {
+  long long base = 0;
+  for (int b0 = 0; b0 < a.B; b0 += 32) {
+    const int b = b0 + lane;
+    int t0 = 0, n = 0;
+    if (b < a.B) n = seq_tiles(a, b, &t0);
+    long long incl = (long long)n * a.Hkv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (b < a.B) {
+      const long long first = base + incl - (long long)n * a.Hkv;
+      if (a.item_tiles)
+        for (int g = 0; g < a.Hkv; ++g) a.item_tiles[(long long)b * a.Hkv + g] = first + (long long)g * n;
+      if (n == 0) {
+        float4* o = reinterpret_cast<float4*>(a.out + (long long)b * a.Hq * D);
+        for (int i = 0; i < a.Hq * D / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0 && a.item_tiles) a.item_tiles[(long long)a.B * a.Hkv] = base;
+}
+
+__device__ __forceinline__ void advance(const DecodeArgs& a, Cursor& c) {
+  if (++c.k < c.n) return;
+  c.k = 0;
+  if (++c.g < a.Hkv) return;
+  c.g = 0;
+  do {
+    if (++c.b >= a.B) { c.n = 0; return; }
+    c.n = seq_tiles(a, c.b, &c.t0);
+  } while (c.n == 0);
+}
+
+template <int MODE, int D, int G>
+__global__ void __launch_bounds__(WARPS * 32)
+    decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap) {
+  using C = Cfg<MODE, D>;
+  using LY = Layout<MODE, D, G>;
+  constexpr int NS = C::NS;
+  constexpr int NPART = C::BF ? 3 : 2;                       // terms of the P' split
+  constexpr bool PACKED = G * NPART <= 8;                    // all terms in one PV tile
+  constexpr int NT = PACKED ? 1 : NPART;                     // PV column tiles
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lg = lane >> 2, lt = lane & 3;       // fragment row group / column pair
+  const int wid = blockIdx.x * WARPS + warp;
+  if (wid >= a.workers) return;                  // no CTA-wide barrier anywhere below
+
+  uint8_t* wcodes = smem + warp * LY::ring;
+  uint8_t* waux = smem + WARPS * LY::ring + warp * LY::aux;
+  float* wscales = reinterpret_cast<float*>(waux);
+  uint16_t* qst = reinterpret_cast<uint16_t*>(waux + LY::scales);
+  uint64_t* wbars = reinterpret_cast<uint64_t*>(waux + LY::scales + LY::q);
+
+  // ---- this warp's share of the tile list
+  Cursor cc;
+  cc.b = cc.g = cc.k = cc.n = cc.t0 = 0;
+  const long long T = scan_tiles(a, -1, &cc, lane);
+  if (wid == 0) publish_items<G, D>(a, lane);
+  const long long my0 = (long long)wid * T / a.workers;
+  const long long my1 = (long long)(wid + 1) * T / a.workers;
+  const int ntiles = (int)(my1 - my0);
+  if (ntiles <= 0) return;
+  scan_tiles(a, my0, &cc, lane);
+  Cursor cp = cc;                                 // producer cursor, NS tiles ahead
+
+  if (lane < NS) mbar_init(&wbars[lane], 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncwarp();
+
+  unsigned valid_mask = 0;        // bit s: stage s holds a fetched tile
+  // Copies of the warp's j-th tile (cursor p) into stage j % NS.
+  auto issue = [&](int j, const Cursor& p) {
+    const int st = j % NS;
+    const int pos0 = (p.t0 + p.k) * TILE;
+    const int blk = a.block_table[(long long)p.b * a.max_blocks + pos0 / a.bs];
+    if (blk >= 0 && blk < a.num_blocks) {
+      if (lane == 0) {
+        const long long cell = ((long long)blk * a.Hkv + p.g) * a.bs + (pos0 % a.bs);
+        const int row = (int)((cell * C::RB) >> 7);
+        uint64_t* bar = &wbars[st];
+        mbar_expect_tx(bar, 2 * C::TB + C::SCALES);
+        uint8_t* kd = wcodes + st * C::STAGE;
+        tma_tile_2d(kd, &kmap, 0, row, bar);
+        tma_tile_2d(kd + C::TBP, &vmap, 0, row, bar);
+        if constexpr (C::DYN) {
+          bulk_copy(wscales + st * 32, a.k_cs + cell, 64, bar);
+          bulk_copy(wscales + st * 32 + 16, a.v_cs + cell, 64, bar);
+        }
+      }
+      valid_mask |= 1u << st;
+    } else {
+      // nothing is fetched, but the stage's phase must still complete so
+      // that the parity of its later uses stays in step
+      if (lane == 0) {
+        atomicOr(a.err, ERR_BAD_INDEX);
+        mbar_arrive(&wbars[st]);
+      }
+      valid_mask &= ~(1u << st);
+    }
+  };
+  for (int j = 0; j < NS && j < ntiles; ++j) {
+    issue(j, cp);
+    advance(a, cp);
+  }
+
+  float ks_static = 1.f, vs_static = 1.f;
+  if constexpr (MODE == FP8_PER_TENSOR) { ks_static = a.k_scale[0]; vs_static = a.v_scale[0]; }
+  // (per-head scales are read per segment below)
+
+  // ---- per-segment state
+  uint32_t qf[C::KSTEPS][2];
+  float s_fac = 0.f;
+  float m_run[2], l_run[2];
+  float acc[NT][C::MTILES][4];
+  int vexp = -1000;               // running max exponent of the V scales (dynamic)
+  int seg_b = -1, seg_g = -1, seg_k0 = 0, seg_klast = 0, seg_n = 0;
+  const int src_t = PACKED ? ((2 * lt) % G) / 2 : lt;   // QK lane column of a PV column's head
+
+  // Writes the segment's result: final output if it covered the whole item,
+  // else a partial at slot (item + worker) for the merge.
+  auto finalize = [&]() {
+    float vsg = vs_static;
+    if constexpr (MODE == FP8_PER_HEAD) vsg = a.v_scale[seg_g];
+    // reduce l over the row groups (m is already uniform across them)
+    float l_tot[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float v = l_run[c];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      l_tot[c] = v;
+    }
+    // fold the split terms onto the lanes that own head columns
+    float o[C::MTILES][4];
+#pragma unroll
+    for (int i = 0; i < C::MTILES; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = 0.f;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) v += acc[n][i][e];
+        if constexpr (PACKED && G >= 2) {
+#pragma unroll
+          for (int k = 1; k < NPART; ++k) v += __shfl_down_sync(0xffffffffu, v, k * (G / 2));
+        }
+        o[i][e] = v;
+      }
+    if constexpr (PACKED && G == 1) {
+      // head 0: columns 0 and 1 in lane column 0, column 2 (bf16) in lane column 1
+#pragma unroll
+      for (int i = 0; i < C::MTILES; ++i) {
+        const float x0 = (C::BF) ? __shfl_down_sync(0xffffffffu, o[i][0], 1) : 0.f;
+        const float x2 = (C::BF) ? __shfl_down_sync(0xffffffffu, o[i][2], 1) : 0.f;
+        o[i][0] += o[i][1] + x0;
+        o[i][2] += o[i][3] + x2;
+      }
+    }
+    float unscale;
+    if constexpr (C::BF) unscale = 1.f;
+    else if constexpr (C::DYN) unscale = pow2i(vexp - 13);
+    else unscale = vsg * (1.f / 16384.f);
+    const int nh = (G == 1) ? 1 : 2;              // heads owned by this lane column
+    const bool owner = (G == 1) ? (lt == 0) : (2 * lt < G);
+    const bool full = (seg_k0 == 0 && seg_klast == seg_n - 1);
+    const int item = seg_b * a.Hkv + seg_g;
+    if (owner) {
+#pragma unroll
+      for (int e1 = 0; e1 < 2; ++e1) {
+        if (e1 >= nh) break;
+        const int h = (G == 1) ? 0 : 2 * lt + e1;
+        const float l = l_tot[e1];
+        const float f = full ? (l > 0.f ? unscale / l : 0.f) : unscale;
+        float* dst = full ? a.out + (((long long)seg_b * a.Hq + seg_g * G + h) * D)
+                          : a.ws_o + (((long long)(item + wid) * G + h) * D);
+#pragma unroll
+        for (int i = 0; i < C::MTILES; ++i) {
+          const int d = lg * (D / 8) + 2 * i;
+          *reinterpret_cast<float2*>(dst + d) = make_float2(o[i][e1] * f, o[i][2 + e1] * f);
+        }
+        if (!full && lg == 0) {
+          float* ml = a.ws_ml + 2 * ((long long)(item + wid) * G + h);
+          ml[0] = m_run[e1];
+          ml[1] = l;
+        }
+      }
+    }
+  };
+
+  int fail_at = -1;
+  int L = 0, lo = 0;              // the current item's context length and window start
+  int j = 0;
+  while (j < ntiles) {
+    // ---------------- segment boundary: finish the previous item, start the next
+    if (cc.b != seg_b || cc.g != seg_g) {
+      if (seg_b >= 0) finalize();
+      seg_b = cc.b;
+      seg_g = cc.g;
+      seg_k0 = cc.k;
+      seg_n = cc.n;
+      L = a.context_lens[seg_b];
+      lo = (a.window > 0 && L > a.window) ? L - a.window : 0;
+      __syncwarp();
+      // q of this item -> staging -> power-of-two prescale -> f16 B fragments
+      const uint4* qsrc =
+          reinterpret_cast<const uint4*>(a.q + ((long long)seg_b * a.Hq + seg_g * G) * D);
+      float amax = 0.f;
+      for (int i = lane; i < G * D / 8; i += 32) {
+        const uint4 v = qsrc[i];
+        reinterpret_cast<uint4*>(qst)[i] = v;
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w4[e] << 16)),
+                                   fabsf(__uint_as_float(w4[e] & 0xFFFF0000u))));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      __syncwarp();
+      int qexp = 0;                   // q is scaled by 2^(14 - qexp) for f16
+      if (!C::BF && amax > 0.f)
+        qexp = max(((int)(__float_as_uint(amax) >> 23) & 0xFF) - 127, -100);
+      const float qmul = C::BF ? 1.f : pow2i(14 - qexp);
+      float ks = ks_static;
+      if constexpr (MODE == FP8_PER_HEAD) ks = a.k_scale[seg_g];
+      s_fac = a.qk_scale * ks * (C::BF ? 1.f : pow2i(qexp - 14));
+#pragma unroll
+      for (int s = 0; s < C::KSTEPS; ++s) {
+        float v[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          v[jj] = (lg < G) ? __uint_as_float((uint32_t)qst[lg * D + qk_d<MODE, D>(lt, s, jj)] << 16) * qmul
+                           : 0.f;
+        if constexpr (C::BF) {
+          qf[s][0] = pack_bf16x2(v[0], v[1]);
+          qf[s][1] = pack_bf16x2(v[2], v[3]);
+        } else {
+          qf[s][0] = pack_f16x2(v[0], v[1]);
+          qf[s][1] = pack_f16x2(v[2], v[3]);
+        }
+      }
+      m_run[0] = m_run[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.f;
+      vexp = -1000;
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < C::MTILES; ++i)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[n][i][e] = 0.f;
+    }
+
+    // ---------------- this iteration: tiles j and j+1 when both are in the item
+    const int cnt = (PAIR == 2 && j + 1 < ntiles && cc.k + 1 < cc.n) ? 2 : 1;
+    const int pos0 = (cc.t0 + cc.k) * TILE;
+    bool ok[PAIR];
+    const uint8_t* kt[PAIR];
+    const float* ksc[PAIR];
+#pragma unroll
+    for (int u = 0; u < PAIR; ++u) {
+      const int st = (j + u) % NS;
+      ok[u] = u < cnt && ((valid_mask >> st) & 1u);
+      kt[u] = wcodes + st * C::STAGE;
+      ksc[u] = wscales + st * 32;
+      if (ok[u] && !mbar_wait(&wbars[st], (uint32_t)(((j + u) / NS) & 1))) fail_at = j;
+    }
+    if (fail_at >= 0) break;
+    // whole: every position of the (up to) 32 is retained, so nothing is masked
+    bool all_ok = true;
+#pragma unroll
+    for (int u = 0; u < PAIR; ++u) all_ok = all_ok && (u >= cnt || ok[u]);
+    const bool whole = all_ok && pos0 >= lo && pos0 + cnt * TILE <= L;
+
+    // ---------------- QK: rows lg, lg+8 of each sub-tile
+    float sacc[PAIR][4];
+#pragma unroll
+    for (int u = 0; u < PAIR; ++u) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[u][e] = 0.f;
+      if (ok[u]) qk_tile<MODE, D>(sacc[u], kt[u], lg, lt, qf);
+    }
+
+    // ---------------- scores (log2 units), online softmax over the 32 positions
+    float s_raw[PAIR][4];
+    float vsr[PAIR][2];
+#pragma unroll
+    for (int u = 0; u < PAIR; ++u) {
+      float kf0 = s_fac, kf1 = s_fac;
+      vsr[u][0] = vsr[u][1] = 1.f;
+      if constexpr (C::DYN) {
+        if (ok[u]) {
+          kf0 = s_fac * ksc[u][lg];
+          kf1 = s_fac * ksc[u][lg + 8];
+          vsr[u][0] = ksc[u][16 + lg];
+          vsr[u][1] = ksc[u][16 + lg + 8];
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int pos = pos0 + u * TILE + lg + ((e & 2) ? 8 : 0);
+        const bool v = ok[u] && (whole || (pos >= lo && pos < L)) && (2 * lt + (e & 1)) < G;
+        s_raw[u][e] = v ? sacc[u][e] * (e < 2 ? kf0 : kf1) : -INFINITY;
+      }
+    }
+    float alpha[2], pw[PAIR][4];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float mt = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < PAIR; ++u) mt = fmaxf(mt, fmaxf(s_raw[u][c], s_raw[u][c + 2]));
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+      const float mn = fmaxf(m_run[c], mt);
+      if (mn == -INFINITY) {
+        alpha[c] = 1.f;
+#pragma unroll
+        for (int u = 0; u < PAIR; ++u) pw[u][c] = pw[u][c + 2] = 0.f;
+      } else {
+        alpha[c] = ex2(m_run[c] - mn);
+        float sum = 0.f;
+#pragma unroll
+        for (int u = 0; u < PAIR; ++u) {
+          pw[u][c] = ex2(s_raw[u][c] - mn);
+          pw[u][c + 2] = ex2(s_raw[u][c + 2] - mn);
+          sum += pw[u][c] + pw[u][c + 2];
+        }
+        l_run[c] = l_run[c] * alpha[c] + sum;
+      }
+      m_run[c] = mn;
+    }
+    // V scale and the power-of-two range factor of P'
+    float vfix = 1.f;
+    if constexpr (C::DYN) {
+      int et = -1000;
+#pragma unroll
+      for (int u = 0; u < PAIR; ++u)
+        if (ok[u]) {
+          // rows outside [lo, L) may hold anything: only retained rows count
+          const int p0 = pos0 + u * TILE + lg, p1 = p0 + 8;
+          if (whole || (p0 >= lo && p0 < L)) et = max(et, f32_exp(vsr[u][0]));
+          if (whole || (p1 >= lo && p1 < L)) et = max(et, f32_exp(vsr[u][1]));
+        }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) et = max(et, __shfl_xor_sync(0xffffffffu, et, o));
+      const int vnew = max(vexp, max(et, -100));
+      if (vnew != vexp) vfix = pow2i(vexp - vnew);     // 0 on the first tile (acc is 0)
+      vexp = vnew;
+      const float fv = pow2i(13 - vexp);
+#pragma unroll
+      for (int u = 0; u < PAIR; ++u) {
+        const float f0 = vsr[u][0] * fv, f1 = vsr[u][1] * fv;
+        pw[u][0] *= f0; pw[u][1] *= f0; pw[u][2] *= f1; pw[u][3] *= f1;
+      }
+    } else if constexpr (!C::BF) {
+#pragma unroll
+      for (int u = 0; u < PAIR; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pw[u][e] *= 16384.f;
+    }
+
+    // ---------------- rescale O when a running max or the range factor moved
+    float al_pv[2] = {alpha[0], alpha[1]};
+    if constexpr (PACKED) {
+      const int srcl = lg * 4 + src_t;
+      const float a0 = __shfl_sync(0xffffffffu, alpha[0], srcl);
+      const float a1 = __shfl_sync(0xffffffffu, alpha[1], srcl);
+      al_pv[0] = a0;
+      al_pv[1] = (G == 1) ? a0 : a1;
+    }
+    al_pv[0] *= vfix;
+    al_pv[1] *= vfix;
+    if (__any_sync(0xffffffffu, al_pv[0] != 1.f || al_pv[1] != 1.f)) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < C::MTILES; ++i) {
+          acc[n][i][0] *= al_pv[0];
+          acc[n][i][1] *= al_pv[1];
+          acc[n][i][2] *= al_pv[0];
+          acc[n][i][3] *= al_pv[1];
+        }
+    }
+
+    // ---------------- PV for each sub-tile
+#pragma unroll
+    for (int u = 0; u < PAIR; ++u) {
+      if (!ok[u]) continue;
+      float pr[4] = {pw[u][0], pw[u][1], pw[u][2], pw[u][3]};
+      if constexpr (PACKED) {
+        const int srcl = lg * 4 + src_t;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pr[e] = __shfl_sync(0xffffffffu, pw[u][e], srcl);
+        if constexpr (G == 1) {     // every column of head 0 reads QK column 0
+          pr[1] = pr[0];
+          pr[3] = pr[2];
+        }
+      }
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 2 * lt + (e & 1);
+          const int k = PACKED ? c / G : n;
+          const bool live = PACKED ? (k < NPART) : (c < G);
+          x[e] = live ? split_term<C::BF>(pr[e], k) : 0.f;
+        }
+        uint32_t p0, p1;
+        if constexpr (C::BF) {
+          p0 = pack_bf16x2(x[0], x[1]);
+          p1 = pack_bf16x2(x[2], x[3]);
+        } else {
+          p0 = pack_f16x2(x[0], x[1]);
+          p1 = pack_f16x2(x[2], x[3]);
+        }
+        pb[n][0] = movmatrix_t(p0);       // positions 0..7
+        pb[n][1] = movmatrix_t(p1);       // positions 8..15
+      }
+      const uint8_t* vt = kt[u] + C::TBP;
+      const int pb0 = pos0 + u * TILE;
+      if (whole) {
+        pv_tile<MODE, D, NT, true>(acc, vt, lg, lt, pb, 0, 0, 0);
+      } else {
+        pv_tile<MODE, D, NT, false>(acc, vt, lg, lt, pb, pb0, lo, L);
+      }
+    }
+
+    // ---------------- advance; refill the consumed stages
+#pragma unroll
+    for (int u = 0; u < PAIR; ++u) {
+      if (u >= cnt) break;
+      seg_klast = cc.k;
+      advance(a, cc);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < PAIR; ++u) {
+      if (u >= cnt) break;
+      if (j + u + NS < ntiles) {
+        fence_proxy_async();
+        issue(j + u + NS, cp);
+        advance(a, cp);
+      }
+    }
+    j += cnt;
+  }
+
+  if (fail_at >= 0) {
+    // a wait ran out: flag it, then drain the copies this warp still has in
+    // flight (tiles fail_at .. fail_at+NS-1), each wait bounded again
+    if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+    for (int jj = fail_at; jj < ntiles && jj < fail_at + NS; ++jj)
+      if ((valid_mask >> (jj % NS)) & 1u)
+        (void)mbar_wait(&wbars[jj % NS], (uint32_t)((jj / NS) & 1));
+    return;
+  }
+  finalize();
+}
+
+// Log-sum-exp merge: one CTA per (sequence, KV head) item, one warp per query
+// head of the group.  Items covered by one worker (or by none) were written by
+// the decode kernel; the others combine the partials of their workers.
+template <int D, int G>
+__global__ void __launch_bounds__(32 * G) merge_kernel(const DecodeArgs a) {
+  const int item = blockIdx.x;
+  const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long P = a.item_tiles[item], n = a.item_tiles[item + 1] - P;
+  if (n <= 0) return;
+  const long long T = a.item_tiles[(long long)a.B * a.Hkv];
+  const long long W = a.workers;
+  const long long w0 = ((P + 1) * W - 1) / T;           // worker owning tile P
+  const long long w1 = ((P + n) * W - 1) / T;           // worker owning tile P + n - 1
+  if (w0 == w1) return;
+  const int b = item / a.Hkv, g = item - b * a.Hkv;
+  float acc[D / 32];
+#pragma unroll
+  for (int k = 0; k < D / 32; ++k) acc[k] = 0.f;
+  float M = -INFINITY, lsum = 0.f;
+  // chunks of 32 workers: lane w-w0 holds that worker's (m, l)
+  for (long long c0 = w0; c0 <= w1; c0 += 32) {
+    const long long w = c0 + lane;
+    float m = -INFINITY, l = 0.f;
+    // a worker whose share is empty (more workers than tiles) wrote nothing
+    const bool live = w <= w1 && (w * T) / W != ((w + 1) * T) / W;
+    const long long part = (item + w) * G + j;
+    if (live) {
+      m = a.ws_ml[2 * part];
+      l = a.ws_ml[2 * part + 1];
+    }
+    float cm = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+    const float Mn = fmaxf(M, cm);
+    const float rescale = (M == -INFINITY) ? 0.f : ex2(M - Mn);
+    const float f = live ? ex2(m - Mn) : 0.f;
+    float ls = f * l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    lsum = lsum * rescale + ls;
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) acc[k] *= rescale;
+    const int cnt = (int)min(32LL, w1 - c0 + 1);
+    for (int i = 0; i < cnt; ++i) {
+      const float fi = __shfl_sync(0xffffffffu, f, i);
+      if (fi == 0.f) continue;
+      const float* src = a.ws_o + ((item + c0 + i) * G + j) * D;
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k) acc[k] += fi * src[lane + 32 * k];
+    }
+    M = Mn;
+  }
+  float* out = a.out + ((long long)b * a.Hq + g * G + j) * D;
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+  for (int k = 0; k < D / 32; ++k) out[lane + 32 * k] = acc[k] * inv;
+}
+
+// ------------------------------------------------------------------ host
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+// The layer's code buffer as a 2-D uint8 tensor of 128-byte rows; one box is
+// a 16-position tile of one (block, KV head) page.
+bool make_map(CUtensorMap* m, const void* base, long long total_bytes, int tile_bytes) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)(total_bytes / 128)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, (cuuint32_t)(tile_bytes / 128)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Sets the kernel's dynamic shared-memory limit once per device; returns its
+// resident CTAs per SM (0 on failure).
+template <int MODE, int D, int G>
+int prepare(int* smem_out) {
+  using LY = Layout<MODE, D, G>;
+  const int smem = LY::total;
+  if (smem_out) *smem_out = smem;
+  static int per_sm[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!per_sm[dev]) {
+    auto kern = decode_kernel<MODE, D, G>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, WARPS * 32, smem) !=
+            cudaSuccess || n <= 0)
+      return 0;
+    per_sm[dev] = n;
+  }
+  return per_sm[dev];
 }
 
 template <int MODE, int D, int G>
 cudaError_t launch3(const DecodeArgs& a, cudaStream_t st) {
-  dim3 grid(a.splits, a.Hkv, a.B);
-  decode_kernel<MODE, D, G><<<grid, WARPS * 32, 0, st>>>(a);
+  using C = Cfg<MODE, D>;
+  const long long total = a.num_blocks * a.Hkv * a.bs * (long long)C::RB;
+  CUtensorMap km, vm;
+  if (total > 0) {
+    if (!make_map(&km, a.k_cache, total, C::TB) || !make_map(&vm, a.v_cache, total, C::TB))
+      return cudaErrorInvalidValue;
+  }
+  int smem = 0;
+  if (prepare<MODE, D, G>(&smem) <= 0) return cudaErrorInvalidConfiguration;
+  const int ctas = (a.workers + WARPS - 1) / WARPS;
+  decode_kernel<MODE, D, G><<<ctas, WARPS * 32, smem, st>>>(a, km, vm);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || a.splits == 1) return e;
-  merge_kernel<D, G><<<dim3(a.Hkv, a.B), D, 0, st>>>(a);
+  if (e != cudaSuccess || a.workers <= 1) return e;
+  merge_kernel<D, G><<<a.B * a.Hkv, 32 * G, 0, st>>>(a);
   return cudaGetLastError();
+}
+
+template <int MODE, int D, int G>
+constexpr bool built() {
+  return !(D == 256 && (G == 8 || (MODE == BF16 && G == 4)));
+}
+
+template <int MODE, int D>
+int per_sm2(int G) {
+  switch (G) {
+    case 1: return prepare<MODE, D, 1>(nullptr);
+    case 2: return prepare<MODE, D, 2>(nullptr);
+    case 4:
+      if constexpr (built<MODE, D, 4>()) return prepare<MODE, D, 4>(nullptr);
+      else return 0;
+    case 8:
+      if constexpr (built<MODE, D, 8>()) return prepare<MODE, D, 8>(nullptr);
+      else return 0;
+    default: return 0;
+  }
+}
+
+template <int MODE>
+int per_sm1(int D, int G) {
+  switch (D) {
+    case 64: return per_sm2<MODE, 64>(G);
+    case 128: return per_sm2<MODE, 128>(G);
+    case 256: return per_sm2<MODE, 256>(G);
+    default: return 0;
+  }
 }
 
 template <int MODE, int D>
@@ -290,8 +1128,12 @@ cudaError_t launch2(int G, const DecodeArgs& a, cudaStream_t st) {
   switch (G) {
     case 1: return launch3<MODE, D, 1>(a, st);
     case 2: return launch3<MODE, D, 2>(a, st);
-    case 4: return launch3<MODE, D, 4>(a, st);
-    case 8: return launch3<MODE, D, 8>(a, st);
+    case 4:
+      if constexpr (built<MODE, D, 4>()) return launch3<MODE, D, 4>(a, st);
+      else return cudaErrorInvalidValue;
+    case 8:
+      if constexpr (built<MODE, D, 8>()) return launch3<MODE, D, 8>(a, st);
+      else return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }
@@ -308,9 +1150,26 @@ cudaError_t launch1(int D, int G, const DecodeArgs& a, cudaStream_t st) {
 
 }  // namespace
 
+int decode_ctas_per_sm(int mode, int D, int G) {
+  switch (mode) {
+    case BF16: return per_sm1<BF16>(D, G);
+    case FP8_PER_TENSOR: return per_sm1<FP8_PER_TENSOR>(D, G);
+    case FP8_PER_HEAD: return per_sm1<FP8_PER_HEAD>(D, G);
+    case FP8_PER_TOKEN_HEAD: return per_sm1<FP8_PER_TOKEN_HEAD>(D, G);
+    case INT4_PER_TOKEN_HEAD: return per_sm1<INT4_PER_TOKEN_HEAD>(D, G);
+    default: return 0;
+  }
+}
+
+int decode_warps_per_cta() { return WARPS; }
+
 bool decode_supported(int mode, int D, int G) {
-  return mode >= BF16 && mode <= INT4_PER_TOKEN_HEAD && (D == 64 || D == 128 || D == 256) &&
-         (G == 1 || G == 2 || G == 4 || G == 8);
+  if (!(mode >= BF16 && mode <= INT4_PER_TOKEN_HEAD)) return false;
+  if (!(D == 64 || D == 128 || D == 256)) return false;
+  if (!(G == 1 || G == 2 || G == 4 || G == 8)) return false;
+  // the PV accumulators (D/16 tiles x 4 x column tiles) must fit in registers
+  if (D == 256 && (G == 8 || (mode == BF16 && G == 4))) return false;
+  return true;
 }
 
 cudaError_t launch_decode(int mode, int D, int G, const DecodeArgs& a, cudaStream_t st) {

@@ -42,10 +42,11 @@ struct DecodeArgs {
   const int* block_table;      // [B][max_blocks]
   const int* context_lens;     // [B]
   float* out;                  // [B][Hq][D]
-  float* ws_o;                 // [B][Hkv][S][G][D] unnormalised partial outputs
-  float* ws_ml;                // [B][Hkv][S][G][2] running max (log2 units) and sum
+  float* ws_o;                 // [B*Hkv + workers][G][D] unnormalised partial outputs
+  float* ws_ml;                // [B*Hkv + workers][G][2] running max (log2 units) and sum
+  long long* item_tiles;       // [B*Hkv + 1] first tile of each item in the tile list; T last
   unsigned* err;
-  int B, Hq, Hkv, bs, max_blocks, window, splits;
+  int B, Hq, Hkv, bs, max_blocks, window, workers;
   long long num_blocks;
   float qk_scale;              // softmax_scale * log2(e)
 };
@@ -58,6 +59,9 @@ cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, long long n, cudaS
 // Returns cudaErrorInvalidValue for an unsupported (mode, D, G) combination.
 cudaError_t launch_decode(int mode, int D, int G, const DecodeArgs& a, cudaStream_t st);
 bool decode_supported(int mode, int D, int G);
+// Resident decode CTAs per SM on the current device (0 if unknown: no device).
+int decode_ctas_per_sm(int mode, int D, int G);
+int decode_warps_per_cta();
 
 // Device error word of the current device.
 unsigned* error_word();

@@ -177,8 +177,8 @@ def kvq_calibrate_per_head(ctx: Context, x, scale_out, qmax: float = 448.0,
            "kvq_calibrate_per_head")
 
 
-def kvq_decode_plan(ctx: Context, layer: int, batch: int, max_context: int, num_splits: int = 0):
-    s, w = i32(num_splits), sz()
+def kvq_decode_plan(ctx: Context, layer: int, batch: int, max_context: int, num_workers: int = 0):
+    s, w = i32(num_workers), sz()
     _check(_lib.kvq_decode_plan(ctx, layer, batch, max_context, ctypes.byref(s), ctypes.byref(w)),
            "kvq_decode_plan")
     return s.value, w.value
@@ -186,7 +186,7 @@ def kvq_decode_plan(ctx: Context, layer: int, batch: int, max_context: int, num_
 
 def kvq_decode_attention(ctx: Context, layer: int, q, k_cache, v_cache, block_table,
                          context_lens, out, *, max_context: int, k_scale=None, v_scale=None,
-                         k_cache_scale=None, v_cache_scale=None, num_splits: int = 0,
+                         k_cache_scale=None, v_cache_scale=None, num_workers: int = 0,
                          workspace=None, workspace_bytes: Optional[int] = None,
                          batch: Optional[int] = None, max_blocks_per_seq: Optional[int] = None,
                          stream=None):
@@ -197,7 +197,7 @@ def kvq_decode_attention(ctx: Context, layer: int, q, k_cache, v_cache, block_ta
     _check(_lib.kvq_decode_attention(ctx, layer, _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                      _ptr(k_scale), _ptr(v_scale), _ptr(k_cache_scale),
                                      _ptr(v_cache_scale), _ptr(block_table), mb,
-                                     _ptr(context_lens), B, max_context, _ptr(out), num_splits,
+                                     _ptr(context_lens), B, max_context, _ptr(out), num_workers,
                                      _ptr(workspace), workspace_bytes, _stream(stream)),
            "kvq_decode_attention")
 

@@ -96,24 +96,27 @@ class LayerRun:
             assert np.array_equal(gv.view(np.uint32), vs.view(np.uint32)), "V scales differ"
 
     # ------------------------------------------------------------ decode
-    def decode(self, num_splits: int = 0, context_lens=None, q=None):
+    def decode(self, num_workers: int = 0, context_lens=None, q=None):
+        """GPU decode; the workspace is filled with NaN first so that a partial
+        that is read without having been written shows up."""
         kvq = K()
         w = self.w
         self.q = wl.queries(w, self.device, layer=self.layer) if q is None else q
         cl = self.pg.context_lens if context_lens is None else context_lens
         self.cl = cl
         max_ctx = int(cl.max().item()) if cl.numel() else 0
-        splits, ws_bytes = kvq.kvq_decode_plan(self.ctx, self.layer, w.B, max_ctx, num_splits)
-        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=self.device)
+        workers, ws_bytes = kvq.kvq_decode_plan(self.ctx, self.layer, w.B, max_ctx, num_workers)
+        ws = torch.full((max(ws_bytes, 16) // 4,), float("nan"), dtype=torch.float32,
+                        device=self.device)
         out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.float32, device=self.device)
         kvq.kvq_decode_attention(self.ctx, self.layer, self.q, self.kc, self.vc,
                                  self.pg.block_table, cl, out, max_context=max_ctx,
                                  k_scale=self.k_scale, v_scale=self.v_scale,
                                  k_cache_scale=self.ks, v_cache_scale=self.vs,
-                                 num_splits=splits, workspace=ws)
+                                 num_workers=workers, workspace=ws)
         torch.cuda.synchronize()
         assert kvq.kvq_get_device_error() == 0
-        self.splits = splits
+        self.workers = workers
         return out
 
     def oracle_decode(self, pairs=None):
@@ -159,6 +162,9 @@ class LayerRun:
 def _rows(mode, codes, slot_scales, static, blk, g, off):
     """Dequantized rows (float64 [n, D]) of KV head g at (blk[i], off[i])."""
     c = codes[blk, g, off]                              # [n, row]
+    if c.shape[0] == 0:
+        return np.zeros((0, c.shape[1] * (2 if mode == orc.INT4_PER_TOKEN_HEAD else 1)
+                         // (2 if mode == orc.BF16 else 1)))
     s = None if slot_scales is None else slot_scales[blk, g, off]
     if mode in (orc.FP8_PER_TOKEN_HEAD, orc.INT4_PER_TOKEN_HEAD):
         return orc.dequantize(mode, c[:, None, None, :], s[:, None, None])[:, 0, 0, :]

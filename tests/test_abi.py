@@ -125,12 +125,15 @@ def test_write_rejects_bad_arguments_without_launching():
 
 def test_decode_plan_and_workspace_rules():
     ctx = _ctx([3], Hq=64, Hkv=8, D=128)
-    s, ws = kvq.kvq_decode_plan(ctx, 0, 8, 131072)
-    assert s >= 1 and ws == (0 if s == 1 else 8 * 8 * s * 8 * 130 * 4)
-    s1, ws1 = kvq.kvq_decode_plan(ctx, 0, 8, 131072, num_splits=1)
-    assert (s1, ws1) == (1, 0)
-    s5, ws5 = kvq.kvq_decode_plan(ctx, 0, 8, 131072, num_splits=5)
-    assert (s5, ws5) == (5, 8 * 8 * 5 * 8 * 130 * 4)
+    w, ws = kvq.kvq_decode_plan(ctx, 0, 8, 131072)
+    assert w >= 1 and ws == (0 if w == 1 else (8 * 8 + w) * 8 * 130 * 4 + (8 * 8 + 1) * 8)
+    w1, ws1 = kvq.kvq_decode_plan(ctx, 0, 8, 131072, num_workers=1)
+    assert (w1, ws1) == (1, 0)
+    w5, ws5 = kvq.kvq_decode_plan(ctx, 0, 8, 131072, num_workers=5)
+    assert (w5, ws5) == (5, (8 * 8 + 5) * 8 * 130 * 4 + (8 * 8 + 1) * 8)
+    # a short context never gets more workers than it has 64-position chunks
+    ws_small, _ = kvq.kvq_decode_plan(ctx, 0, 1, 64)
+    assert ws_small <= 8 * 2
     ok = 0x10000000
     L = kvq._lib
     # too-small workspace is refused before launch

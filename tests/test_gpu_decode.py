@@ -30,14 +30,14 @@ ALL_MODES = [orc.BF16, orc.FP8_PER_TENSOR, orc.FP8_PER_HEAD, orc.FP8_PER_TOKEN_H
 
 @pytest.mark.parametrize("name", list(SMALL))
 @pytest.mark.parametrize("mode", ALL_MODES)
-@pytest.mark.parametrize("splits", [1, 3, 0])
-def test_decode_small(name, mode, splits):
+@pytest.mark.parametrize("workers", [1, 3, 37, 0])
+def test_decode_small(name, mode, workers):
     w = SMALL[name]
     for layer in sorted(set([0, w.num_layers - 1])):   # window layer and full layer
         r = LayerRun(w, mode, layer=layer)
         r.write()
-        out = r.decode(num_splits=splits)
-        r.check_decode(out, where=f"{name} mode {mode} layer {layer} splits {r.splits}")
+        out = r.decode(num_workers=workers)
+        r.check_decode(out, where=f"{name} mode {mode} layer {layer} workers {r.workers}")
 
 
 def test_tiny_per_tensor_one_control():
@@ -57,19 +57,19 @@ def test_ragged_and_empty_contexts(mode, window):
                     seed=77)
     r = LayerRun(w, mode)
     r.write()
-    for splits in (1, 4, 0):
-        out = r.decode(num_splits=splits)
+    for workers in (1, 4, 13, 0):
+        out = r.decode(num_workers=workers)
         assert torch.all(out[0] == 0), "empty context must give zeros"
-        r.check_decode(out, where=f"ragged w{window} splits {splits}")
+        r.check_decode(out, where=f"ragged w{window} workers {workers}")
 
 
-def test_shorter_context_than_written_and_split_independence():
+def test_shorter_context_than_written_and_worker_independence():
     # context_lens below the written length: positions past L are never read.
     w = SMALL["llama70b"]
     r = LayerRun(w, orc.FP8_PER_TOKEN_HEAD)
     r.write()
     cl = torch.tensor([1234, 7], dtype=torch.int32, device="cuda")
-    outs = [r.decode(num_splits=s, context_lens=cl) for s in (1, 2, 7, 0)]
+    outs = [r.decode(num_workers=s, context_lens=cl) for s in (1, 2, 7, 100, 0)]
     for o in outs:
         r.check_decode(o)
     for o in outs[1:]:
@@ -86,7 +86,8 @@ def test_bad_block_id_is_reported_and_skipped():
     out = torch.empty(w.B, w.Hq, w.D, device="cuda")
     kvq.kvq_decode_attention(r.ctx, 0, wl.queries(w, "cuda"), r.kc, r.vc, bt,
                              r.pg.context_lens, out, max_context=100, k_cache_scale=r.ks,
-                             v_cache_scale=r.vs, num_splits=1)
+                             v_cache_scale=r.vs, num_workers=1)
+    torch.cuda.synchronize()
     assert kvq.kvq_get_device_error() == kvq.STATUS.index("KVQ_ERR_BAD_INDEX")
     assert torch.isfinite(out).all()
 
