@@ -176,6 +176,37 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
                                 int max_context, float* out, int num_workers, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* Decode attention that allocates nothing and needs no workspace from the
+ * caller.  The pages have no counterpart to this call; it exists for callers
+ * that cannot provide device scratch: code running where no device allocator
+ * may be used (a serving loop that forbids allocations after start-up, a
+ * plugin inside a host process that owns every device buffer) or bindings
+ * that cannot manage device memory at all.
+ *
+ * Arguments and results are those of kvq_decode_attention without
+ * `workspace`/`workspace_bytes`.  The split-K partials live instead in one
+ * static device array of KVQ_FIXED_SCRATCH_BYTES (16 MiB) per GPU, held by
+ * every GPU that loads the library until the process exits.  A call whose
+ * plan (kvq_decode_plan for the same batch, max_context and num_workers)
+ * needs more than that returns KVQ_ERR_WORKSPACE and launches nothing; pass a
+ * smaller num_workers to fit.
+ *
+ * The first call on a device looks the array's address up on that device
+ * (make that device current first; make the first call before any stream
+ * capture).  Every call on a device shares the one array: calls whose GPU
+ * work overlaps (different streams, concurrent host threads) race on it and
+ * must be serialised by the caller.  The array keeps the last call's
+ * contents; no call reads anything it did not write itself. */
+#define KVQ_FIXED_SCRATCH_BYTES (16u * 1024u * 1024u)
+kvq_status kvq_decode_attention_fixed_scratch(const kvq_ctx* ctx, int layer, const void* q,
+                                              const void* k_cache, const void* v_cache,
+                                              const float* k_scale, const float* v_scale,
+                                              const float* k_cache_scale,
+                                              const float* v_cache_scale, const int* block_table,
+                                              int max_blocks_per_seq, const int* context_lens,
+                                              int batch, int max_context, float* out,
+                                              int num_workers, void* stream);
+
 /* The device codec on its own: out[i] = E4M3 code of in[i] (RNE, saturating
  * to +-448), exactly as kvq_cache_write encodes y.  in: device fp32 [n],
  * out: device uint8 [n]. */

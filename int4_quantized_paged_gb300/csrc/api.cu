@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -323,6 +324,59 @@ kvq_status kvq_get_device_error(void* stream) {
   if (v & kvq::ERR_TIMEOUT) return KVQ_ERR_TIMEOUT;
   if (v & kvq::ERR_BAD_INDEX) return KVQ_ERR_BAD_INDEX;
   return KVQ_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- fixed scratch
+// Scratch for kvq_decode_attention_fixed_scratch: a file-scope device array,
+// present on every GPU that loads the library until the process exits.  Host
+// code cannot use the name as an address; the address is looked up once per
+// device with cudaGetSymbolAddress while that device is current.
+static __device__ __align__(256) unsigned char kvq_fixed_scratch[KVQ_FIXED_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_fixed_scratch_mu;
+void* g_fixed_scratch_ptr[64] = {nullptr};
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_decode_attention_fixed_scratch(const kvq_ctx* ctx, int layer, const void* q,
+                                              const void* k_cache, const void* v_cache,
+                                              const float* k_scale, const float* v_scale,
+                                              const float* k_cache_scale,
+                                              const float* v_cache_scale, const int* block_table,
+                                              int max_blocks_per_seq, const int* context_lens,
+                                              int batch, int max_context, float* out,
+                                              int num_workers, void* stream) {
+  kvq_status st = check_layer(ctx, layer);
+  if (st != KVQ_OK) return st;
+  if (batch < 0 || max_context < 0 || num_workers < 0) return KVQ_ERR_INVALID_ARG;
+  // Size check first: a plan whose partials do not fit is refused.
+  int workers = num_workers;
+  size_t need = 0;
+  st = kvq_decode_plan(ctx, layer, batch, max_context, &workers, &need);
+  if (st != KVQ_OK) return st;
+  if (need > (size_t)KVQ_FIXED_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_fixed_scratch_mu);
+    if (!g_fixed_scratch_ptr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, kvq_fixed_scratch) != cudaSuccess || !p) return KVQ_ERR_CUDA;
+      g_fixed_scratch_ptr[dev] = p;
+    }
+    scratch = g_fixed_scratch_ptr[dev];
+  }
+  // Nothing in the scratch needs to start at zero: every partial and offset
+  // the merge reads is written by the decode kernel of the same call.
+  return kvq_decode_attention(ctx, layer, q, k_cache, v_cache, k_scale, v_scale, k_cache_scale,
+                              v_cache_scale, block_table, max_blocks_per_seq, context_lens, batch,
+                              max_context, out, workers, scratch,
+                              (size_t)KVQ_FIXED_SCRATCH_BYTES, stream);
 }
 
 const char* kvq_status_string(kvq_status s) {

@@ -56,6 +56,8 @@ _SIGS = {
     "kvq_decode_plan": (i32, [P, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(sz)]),
     "kvq_decode_attention": (i32, [P, i32, P, P, P, P, P, P, P, P, i32, P, i32, i32, P, i32, P,
                                    sz, P]),
+    "kvq_decode_attention_fixed_scratch": (i32, [P, i32, P, P, P, P, P, P, P, P, i32, P, i32,
+                                                 i32, P, i32, P]),
     "kvq_e4m3_encode": (i32, [P, P, i64, P]),
     "kvq_get_device_error": (i32, [P]),
     "kvq_status_string": (ctypes.c_char_p, [i32]),
@@ -200,6 +202,22 @@ def kvq_decode_attention(ctx: Context, layer: int, q, k_cache, v_cache, block_ta
                                      _ptr(context_lens), B, max_context, _ptr(out), num_workers,
                                      _ptr(workspace), workspace_bytes, _stream(stream)),
            "kvq_decode_attention")
+
+
+def kvq_decode_attention_fixed_scratch(ctx: Context, layer: int, q, k_cache, v_cache,
+                                       block_table, context_lens, out, *, max_context: int,
+                                       k_scale=None, v_scale=None, k_cache_scale=None,
+                                       v_cache_scale=None, num_workers: int = 0,
+                                       batch: Optional[int] = None,
+                                       max_blocks_per_seq: Optional[int] = None, stream=None):
+    """Decode attention with the library's static scratch instead of a caller
+    workspace (see include/kvq.h); nothing is allocated."""
+    B = q.shape[0] if batch is None else batch
+    mb = block_table.shape[1] if max_blocks_per_seq is None else max_blocks_per_seq
+    _check(_lib.kvq_decode_attention_fixed_scratch(
+        ctx, layer, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _ptr(k_cache_scale), _ptr(v_cache_scale), _ptr(block_table), mb, _ptr(context_lens), B,
+        max_context, _ptr(out), num_workers, _stream(stream)), "kvq_decode_attention_fixed_scratch")
 
 
 def kvq_e4m3_encode(x, out, n: Optional[int] = None, stream=None):
