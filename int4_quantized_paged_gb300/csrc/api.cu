@@ -163,6 +163,7 @@ kvq_status kvq_cache_write(const kvq_ctx* ctx, int layer, const void* k_new, con
   if (st != KVQ_OK) return st;
   if (num_tokens < 0) return KVQ_ERR_INVALID_ARG;
   if (num_tokens == 0) return KVQ_OK;
+  if (num_tokens * 2LL * ctx->cfg.num_kv_heads >= (1LL << 31)) return KVQ_ERR_INVALID_ARG;
   const kvq_config& c = ctx->cfg;
   const int mode = ctx->mode[layer];
   const long long HD = (long long)c.num_kv_heads * c.head_dim;
@@ -188,6 +189,7 @@ kvq_status kvq_cache_write(const kvq_ctx* ctx, int layer, const void* k_new, con
   a.T = num_tokens;
   a.Hkv = c.num_kv_heads;
   a.bs = c.block_size;
+  a.bs_shift = __builtin_ctz((unsigned)c.block_size);
   a.num_blocks = c.num_blocks;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
@@ -293,6 +295,7 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
   a.Hq = c.num_q_heads;
   a.Hkv = c.num_kv_heads;
   a.bs = c.block_size;
+  a.bs_shift = __builtin_ctz((unsigned)c.block_size);
   a.max_blocks = max_blocks_per_seq;
   a.window = ctx->window[layer];
   a.workers = workers;

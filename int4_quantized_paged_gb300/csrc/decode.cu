@@ -572,10 +572,10 @@ __global__ void __launch_bounds__(WARPS * 32)
   auto issue = [&](int j, const Cursor& p) {
     const int st = j % NS;
     const int pos0 = (p.t0 + p.k) * TILE;
-    const int blk = a.block_table[(long long)p.b * a.max_blocks + pos0 / a.bs];
+    const int blk = a.block_table[(long long)p.b * a.max_blocks + (pos0 >> a.bs_shift)];
     if (blk >= 0 && blk < a.num_blocks) {
       if (lane == 0) {
-        const long long cell = ((long long)blk * a.Hkv + p.g) * a.bs + (pos0 % a.bs);
+        const long long cell = ((long long)blk * a.Hkv + p.g) * a.bs + (pos0 & (a.bs - 1));
         const int row = (int)((cell * C::RB) >> 7);
         uint64_t* bar = &wbars[st];
         mbar_expect_tx(bar, 2 * C::TB + C::SCALES);

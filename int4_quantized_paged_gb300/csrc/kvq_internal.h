@@ -21,6 +21,7 @@ struct WriteArgs {
   long long T;
   int Hkv;
   int bs;
+  int bs_shift;                // log2(bs)
   long long num_blocks;
   const float* k_scale;        // static modes
   const float* v_scale;
@@ -46,7 +47,7 @@ struct DecodeArgs {
   float* ws_ml;                // [B*Hkv + workers][G][2] running max (log2 units) and sum
   long long* item_tiles;       // [B*Hkv + 1] first tile of each item in the tile list; T last
   unsigned* err;
-  int B, Hq, Hkv, bs, max_blocks, window, workers;
+  int B, Hq, Hkv, bs, bs_shift, max_blocks, window, workers;
   long long num_blocks;
   float qk_scale;              // softmax_scale * log2(e)
 };

@@ -63,69 +63,132 @@ __device__ __forceinline__ float group_max(float v) {
   return v;
 }
 
-// One group of LPV = D/8 lanes per (token, head, K|V) vector.
+// Quantize and store one vector's 8-element slice held by this lane.
+template <int MODE, int D>
+__device__ __forceinline__ void quantize_store(const WriteArgs& a, const uint4 raw, int is_v, int h,
+                                               long long cell, int sub) {
+  constexpr int LPV = D / 8;
+  uint8_t* cache = is_v ? a.v_cache : a.k_cache;
+  if constexpr (MODE == BF16) {
+    reinterpret_cast<uint4*>(cache + cell * (2 * D))[sub] = raw;
+  } else {
+    float x[8];
+    x[0] = bf16_lo(raw.x); x[1] = bf16_hi(raw.x);
+    x[2] = bf16_lo(raw.y); x[3] = bf16_hi(raw.y);
+    x[4] = bf16_lo(raw.z); x[5] = bf16_hi(raw.z);
+    x[6] = bf16_lo(raw.w); x[7] = bf16_hi(raw.w);
+    float s;
+    if constexpr (MODE == FP8_PER_TENSOR) {
+      s = __ldg(is_v ? a.v_scale : a.k_scale);
+    } else if constexpr (MODE == FP8_PER_HEAD) {
+      s = __ldg((is_v ? a.v_scale : a.k_scale) + h);
+    } else {
+      float m = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+      m = group_max<LPV>(m);
+      constexpr float qmax = (MODE == INT4_PER_TOKEN_HEAD) ? 7.0f : 448.0f;
+      // s = RN32(amax / qmax) by the same reciprocal correction as below
+      // (exact for every bf16 amax >= 2^-100); IEEE division under that.
+      constexpr float rq = 1.0f / qmax;                         // RN(1/qmax)
+      if (m >= 0x1p-100f) {
+        const float q0 = __fmul_rn(m, rq);
+        s = __fmaf_rn(__fmaf_rn(-q0, qmax, m), rq, q0);
+      } else {
+        s = (m == 0.f) ? 1.0f : __fdiv_rn(m, qmax);
+      }
+      if (sub == 0) (is_v ? a.v_cs : a.k_cs)[cell] = s;
+    }
+    // y = RN32(x / s).  One correctly rounded reciprocal per vector, then per
+    // element q0 = RN(x r) and the FMA correction q1 = RN(q0 + RN(x - q0 s) r),
+    // which is the correctly rounded quotient while the remainder x - q0 s
+    // is exact (Markstein's theorem: r within half an ulp of 1/s, q0 within
+    // an ulp).  That holds away from fp32 underflow; below the guard the
+    // kernel divides.  Verified equal to IEEE division over every dynamic
+    // scale (every bf16 amax, /448 and /7, every bf16 |x| <= amax) where
+    // the result decides a code, and over random static scales.  With a
+    // static scale the quotient can be huge; past 1e30 it saturates either
+    // way, so the correction is skipped there.  With a dynamic scale
+    // |x/s| <= qmax (1 + 2^-23), so no guard is needed.
+    constexpr bool DYN = (MODE == FP8_PER_TOKEN_HEAD || MODE == INT4_PER_TOKEN_HEAD);
+    float y[8];
+    constexpr float kLo = DYN ? 0x1p-100f : 0x1p-60f;
+    if (s >= kLo && s <= 0x1p100f) {
+      const float r = __frcp_rn(s);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float q0 = __fmul_rn(x[i], r);
+        const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, x[i]), r, q0);
+        y[i] = (DYN || fabsf(q0) < 1e30f) ? q1 : q0;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(x[i], s);
+    }
+    if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
+      uint32_t packed = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) packed |= int4_code(y[i]) << (4 * i);
+      reinterpret_cast<uint32_t*>(cache + cell * (D / 2))[sub] = packed;
+    } else {
+      uint2 o;
+      o.x = e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16);
+      o.y = e4m3x2(y[4], y[5]) | (e4m3x2(y[6], y[7]) << 16);
+      reinterpret_cast<uint2*>(cache + cell * D)[sub] = o;
+    }
+  }
+}
+
+// One group of LPV = D/8 lanes per (token, head, K|V) vector; each group
+// handles UNROLL grid-strided vectors per pass, issuing all their loads
+// before any arithmetic so several 16-byte loads per lane are in flight.
 template <int MODE, int D>
 __global__ void __launch_bounds__(256) write_kernel(WriteArgs a) {
   constexpr int LPV = D / 8;
+  constexpr int UNROLL = 4;
   const long long lane_id = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int sub = threadIdx.x % LPV;
   const long long per_tensor = a.T * a.Hkv;
   const long long n_vec = 2 * per_tensor;
   const long long stride_vec = ((long long)gridDim.x * blockDim.x) / LPV;
-  for (long long vec = lane_id / LPV; vec < n_vec; vec += stride_vec) {
-    const int is_v = vec >= per_tensor;
-    const long long th = is_v ? vec - per_tensor : vec;
-    const long long t = th / a.Hkv;
-    const int h = (int)(th - t * a.Hkv);
-    const long long slot = a.slots[t];
-    if (slot < 0) continue;                                  // whole group agrees
-    if (slot >= a.num_blocks * a.bs) {
-      if (sub == 0 && !is_v && h == 0) atomicOr(a.err, ERR_BAD_INDEX);
-      continue;
+  // vector index -> (tensor, token, head) in 32-bit arithmetic (the host
+  // refuses writes of 2^31 vectors or more)
+  const unsigned per_t = (unsigned)per_tensor, hkv = (unsigned)a.Hkv;
+  for (long long base = lane_id / LPV; base < n_vec; base += UNROLL * stride_vec) {
+    uint4 raw[UNROLL];
+    long long slot[UNROLL];
+    int hh[UNROLL], vv[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const long long vec = base + u * stride_vec;
+      slot[u] = -1;
+      if (vec < n_vec) {
+        const unsigned v32 = (unsigned)vec;
+        const int is_v = v32 >= per_t;
+        const unsigned th = is_v ? v32 - per_t : v32;
+        const unsigned t = th / hkv;
+        const int h = (int)(th - t * hkv);
+        hh[u] = h;
+        vv[u] = is_v;
+        const uint16_t* src = (is_v ? a.v_new : a.k_new) + (long long)t * a.token_stride + (long long)h * D;
+        raw[u] = __ldg(reinterpret_cast<const uint4*>(src) + sub);
+        slot[u] = __ldg(a.slots + t);
+      }
     }
-    const long long blk = slot / a.bs;
-    const int off = (int)(slot - blk * a.bs);
-    const long long cell = (blk * a.Hkv + h) * a.bs + off;
-    const uint16_t* src = (is_v ? a.v_new : a.k_new) + t * a.token_stride + (long long)h * D;
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src) + sub);
-    uint8_t* cache = is_v ? a.v_cache : a.k_cache;
-
-    if constexpr (MODE == BF16) {
-      reinterpret_cast<uint4*>(cache + cell * (2 * D))[sub] = raw;
-    } else {
-      float x[8];
-      x[0] = bf16_lo(raw.x); x[1] = bf16_hi(raw.x);
-      x[2] = bf16_lo(raw.y); x[3] = bf16_hi(raw.y);
-      x[4] = bf16_lo(raw.z); x[5] = bf16_hi(raw.z);
-      x[6] = bf16_lo(raw.w); x[7] = bf16_hi(raw.w);
-      float s;
-      if constexpr (MODE == FP8_PER_TENSOR) {
-        s = __ldg(is_v ? a.v_scale : a.k_scale);
-      } else if constexpr (MODE == FP8_PER_HEAD) {
-        s = __ldg((is_v ? a.v_scale : a.k_scale) + h);
-      } else {
-        float m = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
-        m = group_max<LPV>(m);
-        constexpr float qmax = (MODE == INT4_PER_TOKEN_HEAD) ? 7.0f : 448.0f;
-        s = (m == 0.f) ? 1.0f : __fdiv_rn(m, qmax);
-        if (sub == 0) (is_v ? a.v_cs : a.k_cs)[cell] = s;
+    for (int u = 0; u < UNROLL; ++u) {
+      const long long vec = base + u * stride_vec;
+      if (vec >= n_vec) break;                                // whole group agrees
+      const int is_v = vv[u], h = hh[u];
+      if (slot[u] < 0) continue;                              // whole group agrees
+      if (slot[u] >= a.num_blocks * a.bs) {
+        if (sub == 0 && !is_v && h == 0) atomicOr(a.err, ERR_BAD_INDEX);
+        continue;
       }
-      float y[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(x[i], s);
-      if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
-        uint32_t packed = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) packed |= int4_code(y[i]) << (4 * i);
-        reinterpret_cast<uint32_t*>(cache + cell * (D / 2))[sub] = packed;
-      } else {
-        uint2 o;
-        o.x = e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16);
-        o.y = e4m3x2(y[4], y[5]) | (e4m3x2(y[6], y[7]) << 16);
-        reinterpret_cast<uint2*>(cache + cell * D)[sub] = o;
-      }
+      const long long blk = slot[u] >> a.bs_shift;
+      const int off = (int)(slot[u] & (a.bs - 1));
+      const long long cell = (blk * a.Hkv + h) * a.bs + off;
+      quantize_store<MODE, D>(a, raw[u], is_v, h, cell, sub);
     }
   }
 }
@@ -135,7 +198,7 @@ cudaError_t launch_mode(int D, const WriteArgs& a, cudaStream_t st) {
   const long long lanes_needed = 2 * a.T * a.Hkv * (D / 8);
   const int threads = 256;
   long long blocks = (lanes_needed + threads - 1) / threads;
-  const long long cap = (long long)sm_count() * 8 * 16;     // enough waves, grid-stride beyond
+  const long long cap = (long long)sm_count() * 8 * 4;      // resident blocks x 4; grid-stride beyond
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   switch (D) {

@@ -145,3 +145,44 @@ def test_e4m3_encoder_all_fp32_bit_patterns():
         nan = np.isnan(f)
         assert np.array_equal(got[~nan], ref[~nan]), f"chunk {c}"
         assert np.all((got[nan] & 0x7F) == 0x7F), f"chunk {c} NaN"
+
+
+@pytest.mark.parametrize("mode", [orc.FP8_PER_TOKEN_HEAD, orc.INT4_PER_TOKEN_HEAD])
+def test_dynamic_scale_every_bf16_amax(mode):
+    # One vector per positive finite bf16 amax (all 32639 of them, subnormal to
+    # the largest), with random bf16 elements below it: every dynamic scale
+    # the write can compute, both the reciprocal paths and the division
+    # fallback for tiny amax, bit-exact against the oracle.
+    w = wl.Workload("edges", Hq=8, Hkv=8, D=128, block_size=16, context_lens=(1360, 1360, 1360))
+    r = LayerRun(w, mode)
+    g = torch.Generator().manual_seed(9)
+    T = sum(w.context_lens)
+    amax_bits = torch.arange(1, 0x7F80, dtype=torch.int64)                 # every bf16 > 0
+    amax_bits = torch.cat([amax_bits, amax_bits[:T * w.Hkv - amax_bits.numel()]])
+    k_bits = amax_bits[torch.randperm(amax_bits.numel(), generator=g)]
+    v_bits = amax_bits[torch.randperm(amax_bits.numel(), generator=g)]
+
+    def vectors(ab):
+        amax = (ab.to(torch.int32) << 16).view(torch.float32).reshape(T, w.Hkv, 1)
+        frac = torch.rand(T, w.Hkv, w.D, generator=g) * 2 - 1
+        x = (frac * amax).to(torch.bfloat16)
+        x[..., 5] = (-amax[..., 0]).to(torch.bfloat16)      # the amax, negative, mid-vector
+        return x.cuda()
+    k, v = vectors(k_bits), vectors(v_bits)
+    pos = wl.fill_positions(w)
+    slots = wl.slot_mapping(w, r.pg, pos, "cuda")
+    kvq = K()
+    kvq.kvq_cache_write(r.ctx, 0, k, v, slots, r.kc, r.vc, r.ks, r.vs)
+    torch.cuda.synchronize()
+    kc, vc, ks, vs = orc.alloc_cache(mode, r.pg.num_blocks, w.Hkv, 16, w.D)
+    orc.cache_write(mode, bits(k), bits(v), slots.cpu().numpy(), kc, vc, ks, vs)
+    r.host = (kc, vc, ks, vs)
+    r.check_write()
+
+
+@pytest.mark.parametrize("scale", [2.0 ** -90, 2.0 ** -70, 3.1e-9, 0.0123, 7.5, 2.0 ** 40, 2.0 ** 110])
+def test_static_scale_extremes(scale):
+    w = SMALL["llama8b"]
+    r = LayerRun(w, orc.FP8_PER_TENSOR, per_tensor_scale=scale)
+    r.write()
+    r.check_write()
