@@ -91,6 +91,8 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_ctx** out) {
   const int bs = cfg->block_size;
   if (bs != 16 && bs != 32 && bs != 64 && bs != 128) return KVQ_ERR_UNSUPPORTED;
   if (!(cfg->softmax_scale >= 0.f) || isinf(cfg->softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  // cache cells (block, KV head, slot) are indexed in 32 bits on the device
+  if (cfg->num_blocks * (long long)cfg->num_kv_heads * bs >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
   for (int l = 0; l < cfg->num_layers; ++l) {
     const int m = cfg->layer_mode[l];
     if (m < KVQ_BF16 || m > KVQ_INT4_PER_TOKEN_HEAD) return KVQ_ERR_INVALID_ARG;

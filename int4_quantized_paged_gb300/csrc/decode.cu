@@ -526,8 +526,15 @@ __device__ __forceinline__ void advance(const DecodeArgs& a, Cursor& c) {
   } while (c.n == 0);
 }
 
+// Resident CTAs per SM the register budget is sized for: four (16 warps,
+// <= 128 registers) where the accumulators fit without spilling, else fewer.
 template <int MODE, int D, int G>
-__global__ void __launch_bounds__(WARPS * 32)
+struct MinCtas {
+  static constexpr int value = (D == 256 || G == 8 || (MODE == BF16 && G >= 4)) ? 2 : 4;
+};
+
+template <int MODE, int D, int G>
+__global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap) {
   using C = Cfg<MODE, D>;
@@ -568,15 +575,19 @@ __global__ void __launch_bounds__(WARPS * 32)
   __syncwarp();
 
   unsigned valid_mask = 0;        // bit s: stage s holds a fetched tile
-  // Copies of the warp's j-th tile (cursor p) into stage j % NS.
-  auto issue = [&](int j, const Cursor& p) {
-    const int st = j % NS;
+  int pst = 0;                    // stage the next issued tile goes to
+  // Copies of the next tile (cursor p) into stage pst.  Cell indices fit in
+  // 32 bits (the host refuses caches of 2^31 cells or more).
+  auto issue = [&](const Cursor& p) {
+    const int st = pst;
+    pst = (pst + 1 == NS) ? 0 : pst + 1;
     const int pos0 = (p.t0 + p.k) * TILE;
     const int blk = a.block_table[(long long)p.b * a.max_blocks + (pos0 >> a.bs_shift)];
     if (blk >= 0 && blk < a.num_blocks) {
       if (lane == 0) {
-        const long long cell = ((long long)blk * a.Hkv + p.g) * a.bs + (pos0 & (a.bs - 1));
-        const int row = (int)((cell * C::RB) >> 7);
+        const unsigned cell = ((unsigned)blk * (unsigned)a.Hkv + (unsigned)p.g) * (unsigned)a.bs +
+                              (unsigned)(pos0 & (a.bs - 1));
+        const int row = (int)(((unsigned long long)cell * C::RB) >> 7);
         uint64_t* bar = &wbars[st];
         mbar_expect_tx(bar, 2 * C::TB + C::SCALES);
         uint8_t* kd = wcodes + st * C::STAGE;
@@ -599,7 +610,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
   };
   for (int j = 0; j < NS && j < ntiles; ++j) {
-    issue(j, cp);
+    issue(cp);
     advance(a, cp);
   }
 
@@ -689,6 +700,8 @@ __global__ void __launch_bounds__(WARPS * 32)
   int fail_at = -1;
   int L = 0, lo = 0;              // the current item's context length and window start
   int j = 0;
+  int cst = 0;                    // stage of tile j
+  uint32_t cpar = 0;              // phase parity of stage cst for tile j
   while (j < ntiles) {
     // ---------------- segment boundary: finish the previous item, start the next
     if (cc.b != seg_b || cc.g != seg_g) {
@@ -757,11 +770,12 @@ __global__ void __launch_bounds__(WARPS * 32)
     const float* ksc[PAIR];
 #pragma unroll
     for (int u = 0; u < PAIR; ++u) {
-      const int st = (j + u) % NS;
+      const int st = (cst + u < NS) ? cst + u : cst + u - NS;
+      const uint32_t par = (cst + u < NS) ? cpar : cpar ^ 1u;
       ok[u] = u < cnt && ((valid_mask >> st) & 1u);
       kt[u] = wcodes + st * C::STAGE;
       ksc[u] = wscales + st * 32;
-      if (ok[u] && !mbar_wait(&wbars[st], (uint32_t)(((j + u) / NS) & 1))) fail_at = j;
+      if (ok[u] && !mbar_wait(&wbars[st], par)) fail_at = j;
     }
     if (fail_at >= 0) break;
     // whole: every position of the (up to) 32 is retained, so nothing is masked
@@ -938,20 +952,23 @@ __global__ void __launch_bounds__(WARPS * 32)
       if (u >= cnt) break;
       if (j + u + NS < ntiles) {
         fence_proxy_async();
-        issue(j + u + NS, cp);
+        issue(cp);
         advance(a, cp);
       }
     }
     j += cnt;
+    cst += cnt;
+    if (cst >= NS) { cst -= NS; cpar ^= 1u; }
   }
 
   if (fail_at >= 0) {
     // a wait ran out: flag it, then drain the copies this warp still has in
     // flight (tiles fail_at .. fail_at+NS-1), each wait bounded again
     if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
-    for (int jj = fail_at; jj < ntiles && jj < fail_at + NS; ++jj)
-      if ((valid_mask >> (jj % NS)) & 1u)
-        (void)mbar_wait(&wbars[jj % NS], (uint32_t)((jj / NS) & 1));
+    for (int jj = fail_at, st = cst, par = (int)cpar; jj < ntiles && jj < fail_at + NS; ++jj) {
+      if ((valid_mask >> st) & 1u) (void)mbar_wait(&wbars[st], (uint32_t)par);
+      if (++st == NS) { st = 0; par ^= 1; }
+    }
     return;
   }
   finalize();
@@ -1000,12 +1017,23 @@ __global__ void __launch_bounds__(32 * G) merge_kernel(const DecodeArgs a) {
 #pragma unroll
     for (int k = 0; k < D / 32; ++k) acc[k] *= rescale;
     const int cnt = (int)min(32LL, w1 - c0 + 1);
-    for (int i = 0; i < cnt; ++i) {
-      const float fi = __shfl_sync(0xffffffffu, f, i);
-      if (fi == 0.f) continue;
-      const float* src = a.ws_o + ((item + c0 + i) * G + j) * D;
+    for (int i0 = 0; i0 < cnt; i0 += 4) {
+      // four partials' loads in flight at once; missing ones read slot c0
+      float v[4][D / 32], fi[4];
 #pragma unroll
-      for (int k = 0; k < D / 32; ++k) acc[k] += fi * src[lane + 32 * k];
+      for (int u = 0; u < 4; ++u) {
+        fi[u] = __shfl_sync(0xffffffffu, f, (i0 + u) & 31);
+        const long long ii = (i0 + u < cnt) ? i0 + u : 0;
+        if (i0 + u >= cnt) fi[u] = 0.f;
+        const float* src = a.ws_o + ((item + c0 + ii) * G + j) * D;
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) v[u][k] = src[lane + 32 * k];
+      }
+      // a slot of an empty or missing share may hold anything: select, not 0 x
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) acc[k] = fi[u] != 0.f ? fmaf(fi[u], v[u][k], acc[k]) : acc[k];
     }
     M = Mn;
   }
