@@ -34,7 +34,6 @@ sys.path.insert(0, ROOT)
 FALLBACK_HBM_GBS = 6800.0
 METRIC = ("FP8-KV decode attention GB/s and KV-tokens/s (% of HBM roofline); "
           "cache-write GB/s")
-WORKLOAD = "llama8b"
 
 
 # ------------------------------------------------------------------ ranks
@@ -184,75 +183,140 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ GPU arm
-def run_gpu(args):
+WORKLOADS = {
+    "llama8b": "llama8b-like decode step: Hq=32 Hkv=8 D=128 block 16, batch 64 x context 4096, "
+               "1 layer, 1 query/seq",
+    "llama70b_128k": "70B-like long-context decode step: Hq=64 Hkv=8 D=128 block 16, batch 8 x "
+                     "context 131072, 1 layer",
+    "gptoss20b": "gpt-oss-20b-like 24-layer decode step: layers alternate window 128 / full, Hq=64 "
+                 "Hkv=8 D=64 block 16, batch 16 x context 32768",
+    "gemma_d256": "Gemma-like decode step: 2 layers (window 512, full), Hq=16 Hkv=8 D=256 block "
+                  "16, batch 32 x context 16384",
+}
+
+
+def rank_workload(name: str, rank: int):
+    """The workload a rank runs: the same shapes, its own seed (the path
+    shards by sequence, so each replica draws its own batch)."""
+    import dataclasses
+    from int4_quantized_paged_gb300 import workloads as wl
+    base = wl.CONFIGS[name]
+    return dataclasses.replace(base, seed=base.seed + 1000 * rank)
+
+
+def layer_modes(w, mode: int, skip_sliding: bool):
+    """Per-layer cache mode: the chosen mode, or BF16 for window layers when
+    the sliding layers are skipped."""
+    return [0 if (skip_sliding and win > 0) else mode for win in w.windows]
+
+
+def setup_gpu(args, dev, rank):
+    """Caches of every layer filled with the context minus the current token,
+    the step's inputs, workspaces.  Returns a dict of state."""
     import torch
     from int4_quantized_paged_gb300 import kvq
     from int4_quantized_paged_gb300 import workloads as wl
+
+    w = rank_workload(args.workload, rank)
+    L = w.context_lens[0]
+    modes = layer_modes(w, kvq.MODE_NAMES[args.mode], args.skip_sliding)
+    pg = wl.paging(w, dev)
+    ctx = kvq.kvq_create(w.num_layers, w.Hq, w.Hkv, w.D, w.block_size, pg.num_blocks, modes,
+                         list(w.windows))
+    layers = []
+    fill_ms = None
+    for li, (mode, win) in enumerate(zip(modes, w.windows)):
+        kc, vc, ks, vs = kvq.alloc_layer_cache(ctx, li, dev)
+        k_scale = v_scale = None
+        if mode == kvq.FP8_PER_TENSOR:
+            k_scale = torch.ones(1, device=dev)
+            v_scale = torch.ones(1, device=dev)
+        elif mode == kvq.FP8_PER_HEAD:
+            ck, cv = wl.calibration_sample(w, dev, layer=li)
+            k_scale = torch.empty(w.Hkv, device=dev)
+            v_scale = torch.empty(w.Hkv, device=dev)
+            kvq.kvq_calibrate_per_head(ctx, ck, k_scale)
+            kvq.kvq_calibrate_per_head(ctx, cv, v_scale)
+        # fill: every retained position but the current one
+        lo = max(0, L - win) if win > 0 else 0
+        pos = [torch.arange(lo, L, dtype=torch.int64) for _ in range(w.B)]
+        T = sum(len(p) for p in pos)
+        k_all, v_all = wl.kv_tokens(w, T, dev, layer=li)
+        slots_all = wl.slot_mapping(w, pg, pos, dev)
+
+        def fill():
+            kvq.kvq_cache_write(ctx, li, k_all, v_all, slots_all, kc, vc, ks, vs, k_scale, v_scale)
+
+        fill()
+        if fill_ms is None and win == 0:
+            # prefill-shaped write of the whole context of one full layer
+            for _ in range(3):
+                fill()
+            torch.cuda.synchronize()
+            ts = []
+            stream = torch.cuda.current_stream()
+            for _ in range(10):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fill()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            fill_ms = (statistics.median(ts), T, mode)
+        n_per = L - lo
+        idx = torch.tensor([b * n_per + n_per - 1 for b in range(w.B)], device=dev)
+        k_new, v_new = k_all[idx].contiguous(), v_all[idx].contiguous()
+        del k_all, v_all, slots_all
+        q = wl.queries(w, dev, layer=li)
+        out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
+        workers, ws_bytes = kvq.kvq_decode_plan(ctx, li, w.B, L, args.workers)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        layers.append(dict(mode=mode, window=win, kc=kc, vc=vc, ks=ks, vs=vs, k_scale=k_scale,
+                           v_scale=v_scale, k_new=k_new, v_new=v_new, q=q, out=out,
+                           workers=workers, ws=ws))
+    slots_new = wl.slot_mapping(w, pg, [torch.tensor([L - 1]) for _ in range(w.B)], dev)
+    torch.cuda.synchronize()
+    return dict(w=w, L=L, pg=pg, ctx=ctx, layers=layers, slots_new=slots_new, fill=fill_ms)
+
+
+def launch_layer(st, li, ev=None, stream=None, inputs=None):
+    """One layer of the decode step: write the current token, then decode."""
+    from int4_quantized_paged_gb300 import kvq
+    lay = st["layers"][li]
+    q, kn, vn, sl, bt, cl = inputs if inputs is not None else (
+        lay["q"], lay["k_new"], lay["v_new"], st["slots_new"], st["pg"].block_table,
+        st["pg"].context_lens)
+    if ev is not None:
+        ev[0].record(stream)
+    kvq.kvq_cache_write(st["ctx"], li, kn, vn, sl, lay["kc"], lay["vc"], lay["ks"], lay["vs"],
+                        lay["k_scale"], lay["v_scale"])
+    if ev is not None:
+        ev[1].record(stream)
+    kvq.kvq_decode_attention(st["ctx"], li, q, lay["kc"], lay["vc"], bt, cl, lay["out"],
+                             max_context=st["L"], k_scale=lay["k_scale"], v_scale=lay["v_scale"],
+                             k_cache_scale=lay["ks"], v_cache_scale=lay["vs"],
+                             num_workers=lay["workers"], workspace=lay["ws"])
+    if ev is not None:
+        ev[2].record(stream)
+
+
+def run_gpu(args):
+    import torch
+    from int4_quantized_paged_gb300 import kvq
 
     rank, world, local = rank_env()
     torch.cuda.set_device(local)
     dist = init_dist("nccl")
     dev = f"cuda:{local}"
-    mode = kvq.MODE_NAMES[args.mode]
-    base = wl.CONFIGS[WORKLOAD]
-    w = wl.Workload(**{**base.__dict__, "seed": base.seed + 1000 * rank})
-    L = w.context_lens[0]
-    pg = wl.paging(w, dev)
-    ctx = kvq.kvq_create(1, w.Hq, w.Hkv, w.D, w.block_size, pg.num_blocks, [mode])
-    kc, vc, ks, vs = kvq.alloc_layer_cache(ctx, 0, dev)
-    k_scale = v_scale = None
-    if mode == kvq.FP8_PER_TENSOR:
-        k_scale = torch.ones(1, device=dev)
-        v_scale = torch.ones(1, device=dev)
-    elif mode == kvq.FP8_PER_HEAD:
-        ck, cv = wl.calibration_sample(w, dev)
-        k_scale = torch.empty(w.Hkv, device=dev)
-        v_scale = torch.empty(w.Hkv, device=dev)
-        kvq.kvq_calibrate_per_head(ctx, ck, k_scale)
-        kvq.kvq_calibrate_per_head(ctx, cv, v_scale)
-
-    # whole-context fill (also the prefill-shaped write measurement)
-    pos = wl.fill_positions(w)
-    T_fill = sum(len(p) for p in pos)
-    k_all, v_all = wl.kv_tokens(w, T_fill, dev)
-    slots_all = wl.slot_mapping(w, pg, pos, dev)
+    st = setup_gpu(args, dev, rank)
+    w, L, layers = st["w"], st["L"], st["layers"]
+    nl = len(layers)
     stream = torch.cuda.current_stream()
+    use_graph = args.graph if args.graph is not None else nl > 1
 
-    def fill():
-        kvq.kvq_cache_write(ctx, 0, k_all, v_all, slots_all, kc, vc, ks, vs, k_scale, v_scale)
-
-    for _ in range(3):
-        fill()
-    torch.cuda.synchronize()
-    fill_ms = []
-    for _ in range(10):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        fill()
-        e1.record(stream)
-        e1.synchronize()
-        fill_ms.append(e0.elapsed_time(e1))
-    fill_ms_med = statistics.median(fill_ms)
-    wb_fill = write_bytes(w, mode, T_fill)
-
-    # the decode step: the current token (position L-1) of each sequence
-    last = [torch.tensor([L - 1]) for _ in range(w.B)]
-    idx = torch.tensor([sum(w.context_lens[:b]) + L - 1 for b in range(w.B)], device=dev)
-    k_new, v_new = k_all[idx].contiguous(), v_all[idx].contiguous()
-    slots_new = wl.slot_mapping(w, pg, last, dev)
-    del k_all, v_all, slots_all
-    q = wl.queries(w, dev)
-    out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
-    workers, ws_bytes = kvq.kvq_decode_plan(ctx, 0, w.B, L, args.workers)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    launches_per_step = 3          # write, decode, merge
-
-    def step(qt=q, kn=k_new, vn=v_new, sl=slots_new, bt=pg.block_table, cl=pg.context_lens,
-             o=out):
-        kvq.kvq_cache_write(ctx, 0, kn, vn, sl, kc, vc, ks, vs, k_scale, v_scale)
-        kvq.kvq_decode_attention(ctx, 0, qt, kc, vc, bt, cl, o, max_context=L, k_scale=k_scale,
-                                 v_scale=v_scale, k_cache_scale=ks, v_cache_scale=vs,
-                                 num_workers=workers, workspace=ws)
+    def step():
+        for li in range(nl):
+            launch_layer(st, li)
 
     for _ in range(args.warmup):
         step()
@@ -260,8 +324,34 @@ def run_gpu(args):
     if kvq.kvq_get_device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
+    # per-kernel times: un-graphed steps with events around each launch
     n = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nl)]
+          for _ in range(n if not use_graph else min(n, 10))]
+    torch.cuda.synchronize()
+    for i in range(len(ev)):
+        for li in range(nl):
+            launch_layer(st, li, ev[i][li], stream)
+    torch.cuda.synchronize()
+    write_ms = [[ev[i][li][0].elapsed_time(ev[i][li][1]) for i in range(len(ev))] for li in range(nl)]
+    dec_ms = [[ev[i][li][1].elapsed_time(ev[i][li][2]) for i in range(len(ev))] for li in range(nl)]
+
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream()
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            step()                                # warm the capture stream
+            torch.cuda.synchronize()
+            with torch.cuda.graph(graph, stream=s2):
+                step()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    # the timed region
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -271,45 +361,48 @@ def run_gpu(args):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(n):
-        ev[i][0].record(stream)
-        kvq.kvq_cache_write(ctx, 0, k_new, v_new, slots_new, kc, vc, ks, vs, k_scale, v_scale)
-        ev[i][1].record(stream)
-        kvq.kvq_decode_attention(ctx, 0, q, kc, vc, pg.block_table, pg.context_lens, out,
-                                 max_context=L, k_scale=k_scale, v_scale=v_scale,
-                                 k_cache_scale=ks, v_cache_scale=vs, num_workers=workers,
-                                 workspace=ws)
-        ev[i][2].record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(dist, local)
     total_ms = t0.elapsed_time(t1)
     clocks = sampler.stop()
-    write_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
-    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
     if kvq.kvq_get_device_error() != 0:
         raise RuntimeError("device error word set during the timed steps")
 
-    # end to end through the C ABI with host buffers
+    # end to end through the C ABI with host buffers (un-graphed calls)
     pin = lambda t: t.cpu().pin_memory()
-    h_in = [pin(x) for x in (q, k_new, v_new, slots_new, pg.block_table, pg.context_lens)]
-    d_in = [torch.empty_like(x, device=dev) for x in h_in]
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in h_in)
-    d2h = h_out.numel() * h_out.element_size()
-    for _ in range(args.warmup):
-        for d, h in zip(d_in, h_in):
+    shared = [st["slots_new"], st["pg"].block_table, st["pg"].context_lens]
+    h_in = [[pin(lay[k]) for k in ("q", "k_new", "v_new")] for lay in layers]
+    h_sh = [pin(x) for x in shared]
+    d_in = [[torch.empty_like(x, device=dev) for x in row] for row in h_in]
+    d_sh = [torch.empty_like(x, device=dev) for x in h_sh]
+    h_out = [torch.empty(lay["out"].shape, dtype=torch.float32).pin_memory() for lay in layers]
+    h2d = sum(x.numel() * x.element_size() for row in h_in for x in row) + \
+        sum(x.numel() * x.element_size() for x in h_sh)
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+
+    def e2e_step():
+        for d, h in zip(d_sh, h_sh):
             d.copy_(h, non_blocking=True)
-        step(*d_in, o=out)
-        h_out.copy_(out, non_blocking=True)
+        for li in range(nl):
+            for d, h in zip(d_in[li], h_in[li]):
+                d.copy_(h, non_blocking=True)
+            launch_layer(st, li, inputs=(d_in[li][0], d_in[li][1], d_in[li][2], d_sh[0],
+                                         d_sh[1], d_sh[2]))
+            h_out[li].copy_(layers[li]["out"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
     torch.cuda.synchronize()
     barrier(dist, local)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(n):
-        for d, h in zip(d_in, h_in):
-            d.copy_(h, non_blocking=True)
-        step(*d_in, o=out)
-        h_out.copy_(out, non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / n
@@ -317,16 +410,23 @@ def run_gpu(args):
     # ---- numbers
     ms_step = max_over_ranks(dist, total_ms / n)
     e2e_ms = max_over_ranks(dist, e2e_ms)
-    dbytes = decode_bytes(w, mode)
-    wbytes = write_bytes(w, mode, w.B)
-    step_bytes = dbytes + wbytes
+    dbytes = [decode_bytes(w, lay["mode"], lay["window"]) for lay in layers]
+    wbytes = [write_bytes(w, lay["mode"], w.B) for lay in layers]
+    step_bytes = sum(dbytes) + sum(wbytes)
     all_bytes = sum_over_ranks(dist, step_bytes)
-    kv_tokens = sum_over_ranks(dist, float(sum(w.context_lens)))
-    dec_avg = statistics.mean(dec_ms)
+    kv_pos = sum(sum(min(Lb, lay["window"]) if lay["window"] else Lb for Lb in w.context_lens)
+                 for lay in layers)
+    kv_tokens = sum_over_ranks(dist, float(kv_pos))
     peak, peak_src = peak_hbm()
-    dec_gbs = dbytes / (dec_avg * 1e-3) / 1e9
-    fill_gbs = wb_fill / (fill_ms_med * 1e-3) / 1e9
-    traffic = profiled_traffic("decode.cu", f"decode_{WORKLOAD}_{args.mode}.md")
+    # dominant kernel: the decode of the layer with the most algorithmic bytes
+    top = max(range(nl), key=lambda li: dbytes[li] * 1e6 + li)
+    dec_avg = statistics.mean(dec_ms[top])
+    dec_gbs = dbytes[top] / (dec_avg * 1e-3) / 1e9
+    fill_ms, fill_T, fill_mode = st["fill"]
+    wb_fill = write_bytes(w, fill_mode, fill_T)
+    fill_gbs = wb_fill / (fill_ms * 1e-3) / 1e9
+    traffic = profiled_traffic("decode.cu", f"decode_{args.workload}_{args.mode}.md")
+    mode_name = args.mode + ("+bf16_sliding" if args.skip_sliding else "")
     res = {
         "metric": METRIC,
         "value": round(all_bytes / (ms_step * 1e-3) / 1e9, 2),
@@ -338,20 +438,20 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3" if mode in (1, 2, 3) else ("int4" if mode == 4 else "bf16"),
-        "data": "synthetic (seeded N(0,1) x per-head log-uniform [0.5,32], 1% tokens x8)",
-        "config": {"workload": "llama8b-like decode step: Hq=32 Hkv=8 D=128 block 16, "
-                               "batch 64 x context 4096, 1 query/seq",
-                   "mode": args.mode, "num_workers": workers,
+        "dtype": {0: "bf16", 4: "int4"}.get(layers[top]["mode"], "fp8_e4m3"),
+        "data": "synthetic (seeded; N(0,1) with the workload's per-head multipliers and outliers)",
+        "config": {"workload": WORKLOADS[args.workload], "mode": mode_name,
+                   "num_workers": layers[top]["workers"], "cuda_graph": bool(graph is not None),
                    "l2": "inputs larger than L2: %.0f MB of cache read per step vs 129 MB L2"
-                         % (dbytes / 1e6),
+                         % (sum(dbytes) / 1e6),
                    "parallelism": f"replicas x{world} (no exchange)"},
         "kv_tokens_per_s": round(kv_tokens / (ms_step * 1e-3), 1),
-        "decode": {"gbs": round(dec_gbs, 2), "ms": round(dec_avg, 5),
-                   "bytes_per_launch": dbytes, "frac_of_peak": round(dec_gbs / peak, 4)},
-        "write_step": {"gbs": round(wbytes / (statistics.mean(write_ms) * 1e-3) / 1e9, 2),
-                       "ms": round(statistics.mean(write_ms), 5), "tokens": w.B},
-        "write_fill": {"gbs": round(fill_gbs, 2), "ms": round(fill_ms_med, 4), "tokens": T_fill,
+        "decode": {"gbs": round(dec_gbs, 2), "ms": round(dec_avg, 5), "layer": top,
+                   "bytes_per_launch": dbytes[top], "frac_of_peak": round(dec_gbs / peak, 4)},
+        "write_step": {"gbs": round(sum(wbytes) / (sum(statistics.mean(x) for x in write_ms) * 1e-3) / 1e9, 2),
+                       "ms": round(sum(statistics.mean(x) for x in write_ms), 5),
+                       "tokens": w.B * nl},
+        "write_fill": {"gbs": round(fill_gbs, 2), "ms": round(fill_ms, 4), "tokens": fill_T,
                        "bytes": wb_fill, "frac_of_peak": round(fill_gbs / peak, 4)},
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
@@ -360,74 +460,105 @@ def run_gpu(args):
         "e2e": {"value": round(all_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
-        "gpu_launches": launches_per_step * n,
+        "gpu_launches": 3 * nl * n,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(args, mode)
+        res["cpu_baseline"] = cpu_baseline(args, kvq.MODE_NAMES[args.mode])
     if dist is not None:
         dist.destroy_process_group()
     return res if rank == 0 else None
 
 
 # ------------------------------------------------------------------ oracle arm
-def oracle_step_setup(mode: int, n_seq: int):
-    """Bounded sample of the same workload for the CPU oracle: n_seq of the 64
-    sequences, their whole 4096-token cache written by the oracle (untimed)."""
+# CPU sample per workload: (sequences, KV heads with all their query heads)
+CPU_SAMPLE = {"llama8b": (8, 8), "llama70b_128k": (1, 1), "gptoss20b": (1, 1), "gemma_d256": (1, 2)}
+
+
+def oracle_step_setup(args, n_seq: int):
+    """Bounded sample of the same workload for the CPU oracle: n_seq of its
+    sequences and the first few KV heads (with all their query heads), every
+    layer; caches written by the oracle (untimed)."""
     import numpy as np
     import torch
     from int4_quantized_paged_gb300 import workloads as wl
+    from int4_quantized_paged_gb300.workloads import MODES
     from oracle import oracle as orc
 
-    base = wl.CONFIGS[WORKLOAD]
+    base = wl.CONFIGS[args.workload]
+    n_seq = min(n_seq or CPU_SAMPLE[args.workload][0], base.B)
+    n_kv = CPU_SAMPLE[args.workload][1]
     w = wl.Workload(**{**base.__dict__, "context_lens": base.context_lens[:n_seq]})
+    modes = layer_modes(w, MODES[args.mode], args.skip_sliding)
     pg = wl.paging(w, "cpu")
-    pos = wl.fill_positions(w)
-    T = sum(len(p) for p in pos)
-    k, v = wl.kv_tokens(w, T, "cpu")
-    slots = wl.slot_mapping(w, pg, pos, "cpu").numpy()
-    u16 = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    kb, vb = u16(k), u16(v)
-    kc, vc, ks, vs = orc.alloc_cache(mode, pg.num_blocks, w.Hkv, w.block_size, w.D)
-    sk = sv = None
-    if mode == 1:
-        sk = sv = np.ones(1, dtype=np.float32)
-    elif mode == 2:
-        ck, cv = wl.calibration_sample(base, "cpu")
-        sk, sv = orc.calibrate_per_head(u16(ck)), orc.calibrate_per_head(u16(cv))
-    orc.cache_write(mode, kb, vb, slots, kc, vc, ks, vs, k_scale=sk, v_scale=sv)
     L = w.context_lens[0]
-    last = np.array([b * L + L - 1 for b in range(w.B)])
-    q = u16(wl.queries(w, "cpu"))
-    st = dict(w=w, pg=pg, kc=kc, vc=vc, ks=ks, vs=vs, sk=sk, sv=sv, q=q,
-              kn=np.ascontiguousarray(kb[last]), vn=np.ascontiguousarray(vb[last]),
-              sl=slots[last], bt=pg.block_table.numpy(), cl=pg.context_lens.numpy())
-    return st
+    u16 = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    layers = []
+    for li, (mode, win) in enumerate(zip(modes, w.windows)):
+        lo = max(0, L - win) if win > 0 else 0
+        pos = [torch.arange(lo, L, dtype=torch.int64) for _ in range(w.B)]
+        T = sum(len(p) for p in pos)
+        k, v = wl.kv_tokens(w, T, "cpu", layer=li)
+        slots = wl.slot_mapping(w, pg, pos, "cpu").numpy()
+        kb, vb = u16(k), u16(v)
+        kc, vc, ks, vs = orc.alloc_cache(mode, pg.num_blocks, w.Hkv, w.block_size, w.D)
+        sk = sv = None
+        if mode == 1:
+            sk = sv = np.ones(1, dtype=np.float32)
+        elif mode == 2:
+            ck, cv = wl.calibration_sample(base, "cpu", layer=li)
+            sk, sv = orc.calibrate_per_head(u16(ck)), orc.calibrate_per_head(u16(cv))
+        orc.cache_write(mode, kb, vb, slots, kc, vc, ks, vs, k_scale=sk, v_scale=sv)
+        n_per = L - lo
+        last = np.array([b * n_per + n_per - 1 for b in range(w.B)])
+        layers.append(dict(mode=mode, window=win, kc=kc, vc=vc, ks=ks, vs=vs, sk=sk, sv=sv,
+                           q=u16(wl.queries(w, "cpu", layer=li)),
+                           kn=np.ascontiguousarray(kb[last]), vn=np.ascontiguousarray(vb[last]),
+                           sl=slots[last]))
+    pairs = [(b, g * w.G + j) for b in range(w.B) for g in range(n_kv) for j in range(w.G)]
+    return dict(w=w, layers=layers, bt=pg.block_table.numpy(), cl=pg.context_lens.numpy(),
+                pairs=pairs, n_kv=n_kv)
 
 
-def oracle_step(mode: int, st) -> None:
+def oracle_step(st) -> None:
     from oracle import oracle as orc
-    orc.cache_write(mode, st["kn"], st["vn"], st["sl"], st["kc"], st["vc"], st["ks"], st["vs"],
-                    k_scale=st["sk"], v_scale=st["sv"])
-    orc.decode(mode, st["q"], st["kc"], st["vc"], st["bt"], st["cl"], k_scale=st["sk"],
-               v_scale=st["sv"], k_cache_scale=st["ks"], v_cache_scale=st["vs"])
+    for lay in st["layers"]:
+        orc.cache_write(lay["mode"], lay["kn"], lay["vn"], lay["sl"], lay["kc"], lay["vc"],
+                        lay["ks"], lay["vs"], k_scale=lay["sk"], v_scale=lay["sv"])
+        orc.decode(lay["mode"], lay["q"], lay["kc"], lay["vc"], st["bt"], st["cl"],
+                   k_scale=lay["sk"], v_scale=lay["sv"], k_cache_scale=lay["ks"],
+                   v_cache_scale=lay["vs"], window=lay["window"], pairs=st["pairs"])
+
+
+def oracle_bytes(st) -> float:
+    """Algorithmic bytes of the sampled items: decode of n_kv KV heads (and
+    their query heads) of the sampled sequences, write of their new tokens."""
+    import dataclasses
+    w = st["w"]
+    ws = dataclasses.replace(w, Hkv=st["n_kv"], Hq=st["n_kv"] * w.G)
+    return sum(decode_bytes(ws, lay["mode"], lay["window"]) + write_bytes(w, lay["mode"], w.B)
+               for lay in st["layers"])
 
 
 def cpu_baseline(args, mode: int, steps: int = 2):
     from oracle import oracle as orc
-    n_seq = args.cpu_seqs
-    st = oracle_step_setup(mode, n_seq)
-    oracle_step(mode, st)
+    st = oracle_step_setup(args, args.cpu_seqs)
+    oracle_step(st)
     t = time.perf_counter()
     for _ in range(steps):
-        oracle_step(mode, st)
+        oracle_step(st)
     dt = (time.perf_counter() - t) / steps
     w = st["w"]
-    b = decode_bytes(w, mode) + write_bytes(w, mode, w.B)
-    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": orc.num_threads(),
-            "kind": "oracle",
-            "sample": f"{n_seq} of 64 sequences (x 4096 positions, all 32 heads) of the same "
-                      f"decode step; {steps} timed steps of {dt:.2f} s wall each"}
+    return {"value": round(oracle_bytes(st) / dt / 1e9, 4), "unit": "GB/s",
+            "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"{w.B} of {wl_batch(args)} sequences x {st['n_kv']} of {w.Hkv} KV heads "
+                      f"(their query heads, every layer) of the same decode step; {steps} timed "
+                      f"steps of {dt:.2f} s wall each"}
+
+
+def wl_batch(args) -> int:
+    from int4_quantized_paged_gb300 import workloads as wl
+    return wl.CONFIGS[args.workload].B
 
 
 def run_reference(args):
@@ -437,24 +568,23 @@ def run_reference(args):
     from oracle import oracle as orc
     from int4_quantized_paged_gb300.workloads import MODES
     mode = MODES[args.mode]
-    st = oracle_step_setup(mode, args.cpu_seqs)
+    st = oracle_step_setup(args, args.cpu_seqs)
     for _ in range(args.warmup):
-        oracle_step(mode, st)
+        oracle_step(st)
     t = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(mode, st)
+        oracle_step(st)
     dt = (time.perf_counter() - t) / args.steps
+    v = round(oracle_bytes(st) / dt / 1e9, 4)
     w = st["w"]
-    b = decode_bytes(w, mode) + write_bytes(w, mode, w.B)
-    v = round(b / dt / 1e9, 4)
-    sample = (f"{args.cpu_seqs} of 64 sequences (x 4096 positions, all 32 heads) of the "
-              f"llama8b decode step, per step")
+    sample = (f"{w.B} of {wl_batch(args)} sequences x {st['n_kv']} of {w.Hkv} KV heads (their "
+              f"query heads, every layer) of the {args.workload} decode step, per step")
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8_e4m3" if mode in (1, 2, 3) else ("int4" if mode == 4 else "bf16"),
-        "data": "synthetic", "config": {"workload": "llama8b-like decode step (sampled)",
+        "dtype": {0: "bf16", 4: "int4"}.get(mode, "fp8_e4m3"),
+        "data": "synthetic", "config": {"workload": WORKLOADS[args.workload] + " (sampled)",
                                         "mode": args.mode},
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": orc.num_threads(),
                          "kind": "oracle", "sample": sample},
@@ -472,7 +602,13 @@ def main(argv=None):
                     choices=["bf16", "fp8_per_tensor", "fp8_per_head", "fp8_per_token_head",
                              "int4_per_token_head"])
     ap.add_argument("--workers", type=int, default=0)
-    ap.add_argument("--cpu-seqs", type=int, default=8)
+    ap.add_argument("--workload", default="llama8b", choices=sorted(WORKLOADS))
+    ap.add_argument("--skip-sliding", action="store_true",
+                    help="keep the window layers' caches in BF16 (layer skipping)")
+    ap.add_argument("--graph", dest="graph", action="store_true", default=None,
+                    help="replay the step as a CUDA graph (default: on for multi-layer steps)")
+    ap.add_argument("--no-graph", dest="graph", action="store_false")
+    ap.add_argument("--cpu-seqs", type=int, default=0, help="0: the workload's default sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)

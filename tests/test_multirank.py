@@ -1,0 +1,75 @@
+"""Host logic of the N > 1 benchmark path on CPU: two gloo ranks.
+
+The path shards by sequence (replicas only, no data-path collective); what
+the ranks share is the timing protocol: a barrier around the timed region,
+the maximum of the ranks' step times and the sum of their bytes.
+"""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    d = bench.init_dist("gloo")
+    r, ws, lr = bench.rank_env()
+    bench.barrier(d)
+    mx = bench.max_over_ranks(d, 1.5 + rank)          # step times 1.5 and 2.5 ms
+    sm = bench.sum_over_ranks(d, 100.0 * (rank + 1))  # bytes 100 and 200
+    w = bench.rank_workload("llama8b", rank)
+    out[rank] = (r, ws, lr, mx, sm, w.seed)
+    d.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce_times_and_bytes():
+    ctx = mp.get_context("spawn")
+    manager = ctx.Manager()
+    out = manager.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    r0, r1 = out[0], out[1]
+    assert (r0[0], r0[1], r0[2]) == (0, 2, 0) and (r1[0], r1[1], r1[2]) == (1, 2, 1)
+    assert r0[3] == r1[3] == 2.5                      # max over ranks
+    assert r0[4] == r1[4] == 300.0                    # sum over ranks
+    assert r0[5] != r1[5]                             # each replica draws its own batch
+
+
+def test_single_rank_needs_no_process_group(monkeypatch):
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.rank_env() == (0, 1, 0)
+    assert bench.init_dist("gloo") is None
+    assert bench.max_over_ranks(None, 3.0) == 3.0 and bench.sum_over_ranks(None, 4.0) == 4.0
+
+
+def test_byte_accounting_matches_the_pages_per_token_formulas():
+    # decode bytes of one full layer: positions x Hkv x (2 D elem + 8) + q + out + table
+    from int4_quantized_paged_gb300 import workloads as wl
+    w = wl.scaled(wl.CONFIGS["llama8b"], batch=2, context=64)
+    b = bench.decode_bytes(w, 3)
+    assert b == 2 * 64 * 8 * (256 + 8) + 2 * 4 * 4 + 2 * 32 * 128 * 6
+    assert bench.decode_bytes(w, 2) == 2 * 64 * 8 * 256 + 2 * 4 * 4 + 2 * 32 * 128 * 6
+    assert bench.decode_bytes(w, 0, window=16) == 2 * 16 * 8 * 512 + 2 * 4 * 4 + 2 * 32 * 128 * 6
+    # write bytes per token: Hkv x (bf16 K+V in + codes out + scales) + int64 slot
+    assert bench.write_bytes(w, 3, 1) == 8 * (4 * 128 + 2 * 128 + 8) + 8 == 6216
+    assert bench.write_bytes(w, 4, 1) == 8 * (4 * 128 + 128 + 8) + 8
