@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -325,9 +326,9 @@ def run_gpu(args):
         raise RuntimeError("device error word set during warm-up")
 
     # per-kernel times: un-graphed steps with events around each launch
-    n = args.steps
+    n_ev = min(args.steps, 200) if args.steps > 0 else 200
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nl)]
-          for _ in range(n if not use_graph else min(n, 10))]
+          for _ in range(n_ev if not use_graph else min(n_ev, 10))]
     torch.cuda.synchronize()
     for i in range(len(ev)):
         for li in range(nl):
@@ -335,6 +336,10 @@ def run_gpu(args):
     torch.cuda.synchronize()
     write_ms = [[ev[i][li][0].elapsed_time(ev[i][li][1]) for i in range(len(ev))] for li in range(nl)]
     dec_ms = [[ev[i][li][1].elapsed_time(ev[i][li][2]) for i in range(len(ev))] for li in range(nl)]
+    # --steps 0: enough steps for about a second of timed work, so that the
+    # clock samples (every 200 ms) fall inside the loaded region
+    est_ms = sum(statistics.mean(x) for x in write_ms) + sum(statistics.mean(x) for x in dec_ms)
+    n = args.steps if args.steps > 0 else int(min(20000, max(50, math.ceil(1000.0 / est_ms))))
 
     graph = None
     if use_graph:
@@ -354,7 +359,11 @@ def run_gpu(args):
     # the timed region
     sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.3)
+    t_pre = time.time()
+    while time.time() - t_pre < 0.4:      # keep the GPU loaded while the sampler starts
+        for _ in range(max(1, n // 4)):
+            graph.replay() if graph is not None else step()
+        torch.cuda.synchronize()
     barrier(dist, local)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -540,13 +549,17 @@ def oracle_bytes(st) -> float:
                for lay in st["layers"])
 
 
-def cpu_baseline(args, mode: int, steps: int = 2):
+def cpu_baseline(args, mode: int, seconds: float = 10.0):
+    """Times the oracle on a bounded sample for about `seconds` of wall time
+    (at least two steps)."""
     from oracle import oracle as orc
     st = oracle_step_setup(args, args.cpu_seqs)
     oracle_step(st)
     t = time.perf_counter()
-    for _ in range(steps):
+    steps = 0
+    while steps < 2 or time.perf_counter() - t < seconds:
         oracle_step(st)
+        steps += 1
     dt = (time.perf_counter() - t) / steps
     w = st["w"]
     return {"value": round(oracle_bytes(st) / dt / 1e9, 4), "unit": "GB/s",
@@ -571,17 +584,18 @@ def run_reference(args):
     st = oracle_step_setup(args, args.cpu_seqs)
     for _ in range(args.warmup):
         oracle_step(st)
+    steps = args.steps if args.steps > 0 else 5
     t = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(steps):
         oracle_step(st)
-    dt = (time.perf_counter() - t) / args.steps
+    dt = (time.perf_counter() - t) / steps
     v = round(oracle_bytes(st) / dt / 1e9, 4)
     w = st["w"]
     sample = (f"{w.B} of {wl_batch(args)} sequences x {st['n_kv']} of {w.Hkv} KV heads (their "
               f"query heads, every layer) of the {args.workload} decode step, per step")
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {0: "bf16", 4: "int4"}.get(mode, "fp8_e4m3"),
         "data": "synthetic", "config": {"workload": WORKLOADS[args.workload] + " (sampled)",
@@ -595,7 +609,8 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="0: as many steps as take about one second")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--mode", default="fp8_per_token_head",
