@@ -59,8 +59,12 @@ constexpr int WARPS = 4;         // worker warps per CTA (independent)
 #ifndef KVQ_TILES_PER_ITER
 #define KVQ_TILES_PER_ITER 1
 #endif
+#ifndef KVQ_QK2
+#define KVQ_QK2 1              // two independent QK accumulator chains
+#endif
 constexpr int PAIR = KVQ_TILES_PER_ITER;   // 16-position tiles per loop iteration
 constexpr int TILE = 16;         // positions per tile
+constexpr int KP = 13;           // P' = p v_scale 2^(KP - vexp) < 2^14 (dynamic scales)
 constexpr long long SPIN_LIMIT_CYCLES = 4000000000LL;   // about 2 s at 2 GHz
 
 // ------------------------------------------------------------------ PTX
@@ -293,11 +297,17 @@ __device__ __forceinline__ int f32_exp(float x) {
 // QK of one 16-position sub-tile: sacc (rows lg, lg+8; columns 2lt, 2lt+1)
 // += K_tile . Q^T.  The lane reads its D/4-element segment of rows lg, lg+8.
 template <int MODE, int D>
-__device__ __forceinline__ void qk_tile(float sacc[4], const uint8_t* kt, int lg, int lt,
+__device__ __forceinline__ void qk_tile(float sacc_out[4], const uint8_t* kt, int lg, int lt,
                                         const uint32_t (*qf)[2]) {
   constexpr int RB = row_bytes<MODE>(D);
   constexpr int KSTEPS = D / 16;
+  constexpr int NCH = KVQ_QK2 ? 2 : 1;     // independent accumulator chains
   const int r0 = lg, r1 = lg + 8;
+  float sacc2[NCH][4];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sacc2[c][e] = 0.f;
   if constexpr (MODE == BF16) {
 #pragma unroll
     for (int s4 = 0; s4 < KSTEPS; s4 += 2) {
@@ -307,7 +317,7 @@ __device__ __forceinline__ void qk_tile(float sacc[4], const uint8_t* kt, int lg
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const uint32_t af[4] = {w0[2 * u], w1[2 * u], w0[2 * u + 1], w1[2 * u + 1]};
-        mma16816<true>(sacc, af, qf[s4 + u][0], qf[s4 + u][1]);
+        mma16816<true>(sacc2[u % NCH], af, qf[s4 + u][0], qf[s4 + u][1]);
       }
     }
   } else if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
@@ -322,7 +332,7 @@ __device__ __forceinline__ void qk_tile(float sacc[4], const uint8_t* kt, int lg
       const uint32_t x0 = w0[s >> 1] ^ 0x88888888u, x1 = w1[s >> 1] ^ 0x88888888u;
       const uint32_t af[4] = {nib2_f16x2(x0 >> sh), nib2_f16x2(x1 >> sh),
                               nib2_f16x2(x0 >> (sh + 4)), nib2_f16x2(x1 >> (sh + 4))};
-      mma16816<false>(sacc, af, qf[s][0], qf[s][1]);
+      mma16816<false>(sacc2[s % NCH], af, qf[s][0], qf[s][1]);
     }
   } else {
 #pragma unroll
@@ -335,9 +345,15 @@ __device__ __forceinline__ void qk_tile(float sacc[4], const uint8_t* kt, int lg
         uint32_t af[4];
         e4m3x4_f16(w0[u], af[0], af[2]);
         e4m3x4_f16(w1[u], af[1], af[3]);
-        mma16816<false>(sacc, af, qf[s4 + u][0], qf[s4 + u][1]);
+        mma16816<false>(sacc2[u % NCH], af, qf[s4 + u][0], qf[s4 + u][1]);
       }
     }
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float v = sacc2[0][e];
+    if constexpr (NCH == 2) v += sacc2[NCH - 1][e];
+    sacc_out[e] += v;
   }
 }
 
@@ -543,6 +559,9 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
   constexpr int NPART = C::BF ? 3 : 2;                       // terms of the P' split
   constexpr bool PACKED = G * NPART <= 8;                    // all terms in one PV tile
   constexpr int NT = PACKED ? 1 : NPART;                     // PV column tiles
+  // QK columns that carry scores.  PACKED: column c holds head c % G, and its
+  // weight feeds term c / G of the split, so the QK and PV columns coincide.
+  constexpr int NCOL = PACKED ? G * NPART : G;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -550,6 +569,8 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lg = lane >> 2, lt = lane & 3;       // fragment row group / column pair
   const int wid = blockIdx.x * WARPS + warp;
+  // the merge kernel may be scheduled now; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (wid >= a.workers) return;                  // no CTA-wide barrier anywhere below
 
   uint8_t* wcodes = smem + warp * LY::ring;
@@ -576,13 +597,20 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
 
   unsigned valid_mask = 0;        // bit s: stage s holds a fetched tile
   int pst = 0;                    // stage the next issued tile goes to
-  // Copies of the next tile (cursor p) into stage pst.  Cell indices fit in
-  // 32 bits (the host refuses caches of 2^31 cells or more).
-  auto issue = [&](const Cursor& p) {
+  // Block id of the producer cursor's tile, loaded one issue ahead so that its
+  // latency is spent on the previous tile's compute.
+  auto block_of = [&](const Cursor& p) -> int {
+    if (p.n == 0) return -1;      // past the end of the list
+    const int pos0 = (p.t0 + p.k) * TILE;
+    return __ldg(a.block_table + (long long)p.b * a.max_blocks + (pos0 >> a.bs_shift));
+  };
+  int blk_next = block_of(cp);
+  // Copies of the next tile (cursor p, block id blk) into stage pst.  Cell
+  // indices fit in 32 bits (the host refuses caches of 2^31 cells or more).
+  auto issue = [&](const Cursor& p, const int blk) {
     const int st = pst;
     pst = (pst + 1 == NS) ? 0 : pst + 1;
     const int pos0 = (p.t0 + p.k) * TILE;
-    const int blk = a.block_table[(long long)p.b * a.max_blocks + (pos0 >> a.bs_shift)];
     if (blk >= 0 && blk < a.num_blocks) {
       if (lane == 0) {
         const unsigned cell = ((unsigned)blk * (unsigned)a.Hkv + (unsigned)p.g) * (unsigned)a.bs +
@@ -610,8 +638,9 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     }
   };
   for (int j = 0; j < NS && j < ntiles; ++j) {
-    issue(cp);
+    issue(cp, blk_next);
     advance(a, cp);
+    blk_next = block_of(cp);
   }
 
   float ks_static = 1.f, vs_static = 1.f;
@@ -624,8 +653,8 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
   float m_run[2], l_run[2];
   float acc[NT][C::MTILES][4];
   int vexp = -1000;               // running max exponent of the V scales (dynamic)
+  float fv = 0.f;                 // 2^(KP - vexp)
   int seg_b = -1, seg_g = -1, seg_k0 = 0, seg_klast = 0, seg_n = 0;
-  const int src_t = PACKED ? ((2 * lt) % G) / 2 : lt;   // QK lane column of a PV column's head
 
   // Writes the segment's result: final output if it covered the whole item,
   // else a partial at slot (item + worker) for the merge.
@@ -668,7 +697,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     }
     float unscale;
     if constexpr (C::BF) unscale = 1.f;
-    else if constexpr (C::DYN) unscale = pow2i(vexp - 13);
+    else if constexpr (C::DYN) unscale = pow2i(vexp - KP);
     else unscale = vsg * (1.f / 16384.f);
     const int nh = (G == 1) ? 1 : 2;              // heads owned by this lane column
     const bool owner = (G == 1) ? (lt == 0) : (2 * lt < G);
@@ -741,8 +770,9 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
         float v[4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
-          v[jj] = (lg < G) ? __uint_as_float((uint32_t)qst[lg * D + qk_d<MODE, D>(lt, s, jj)] << 16) * qmul
-                           : 0.f;
+          v[jj] = (lg < NCOL)
+                      ? __uint_as_float((uint32_t)qst[(lg % G) * D + qk_d<MODE, D>(lt, s, jj)] << 16) * qmul
+                      : 0.f;
         if constexpr (C::BF) {
           qf[s][0] = pack_bf16x2(v[0], v[1]);
           qf[s][1] = pack_bf16x2(v[2], v[3]);
@@ -754,6 +784,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
       m_run[0] = m_run[1] = -INFINITY;
       l_run[0] = l_run[1] = 0.f;
       vexp = -1000;
+      fv = 0.f;
 #pragma unroll
       for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -793,9 +824,10 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
       if (ok[u]) qk_tile<MODE, D>(sacc[u], kt[u], lg, lt, qf);
     }
 
-    // ---------------- scores (log2 units), online softmax over the 32 positions
+    // ---------------- scores (log2 units); masked entries are -inf
     float s_raw[PAIR][4];
     float vsr[PAIR][2];
+    int et_loc = -1000;             // largest V-scale exponent of this lane's retained rows
 #pragma unroll
     for (int u = 0; u < PAIR; ++u) {
       float kf0 = s_fac, kf1 = s_fac;
@@ -806,59 +838,85 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
           kf1 = s_fac * ksc[u][lg + 8];
           vsr[u][0] = ksc[u][16 + lg];
           vsr[u][1] = ksc[u][16 + lg + 8];
+          // rows outside [lo, L) may hold anything: only retained rows count
+          const int p0 = pos0 + u * TILE + lg, p1 = p0 + 8;
+          if (whole || (p0 >= lo && p0 < L)) et_loc = max(et_loc, f32_exp(vsr[u][0]));
+          if (whole || (p1 >= lo && p1 < L)) et_loc = max(et_loc, f32_exp(vsr[u][1]));
         }
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int pos = pos0 + u * TILE + lg + ((e & 2) ? 8 : 0);
-        const bool v = ok[u] && (whole || (pos >= lo && pos < L)) && (2 * lt + (e & 1)) < G;
+        const bool v = ok[u] && (whole || (pos >= lo && pos < L)) && (2 * lt + (e & 1)) < NCOL;
         s_raw[u][e] = v ? sacc[u][e] * (e < 2 ? kf0 : kf1) : -INFINITY;
       }
     }
-    float alpha[2], pw[PAIR][4];
+
+    // ---------------- online softmax.  The running max m_run (per column,
+    // warp-uniform) and the V-scale exponent vexp only change when some lane
+    // holds a larger value; only then are they reduced over the warp and O
+    // and l rescaled, so most tiles take no shuffle here.
+    float lmax[2];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       float mt = -INFINITY;
 #pragma unroll
       for (int u = 0; u < PAIR; ++u) mt = fmaxf(mt, fmaxf(s_raw[u][c], s_raw[u][c + 2]));
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-      const float mn = fmaxf(m_run[c], mt);
-      if (mn == -INFINITY) {
-        alpha[c] = 1.f;
-#pragma unroll
-        for (int u = 0; u < PAIR; ++u) pw[u][c] = pw[u][c + 2] = 0.f;
-      } else {
-        alpha[c] = ex2(m_run[c] - mn);
-        float sum = 0.f;
-#pragma unroll
-        for (int u = 0; u < PAIR; ++u) {
-          pw[u][c] = ex2(s_raw[u][c] - mn);
-          pw[u][c + 2] = ex2(s_raw[u][c + 2] - mn);
-          sum += pw[u][c] + pw[u][c + 2];
-        }
-        l_run[c] = l_run[c] * alpha[c] + sum;
-      }
-      m_run[c] = mn;
+      lmax[c] = mt;
     }
-    // V scale and the power-of-two range factor of P'
-    float vfix = 1.f;
-    if constexpr (C::DYN) {
-      int et = -1000;
+    bool raise = lmax[0] > m_run[0] || lmax[1] > m_run[1];
+    if constexpr (C::DYN) raise = raise || et_loc > vexp;
+    if (__any_sync(0xffffffffu, raise)) {
+      float al[2];
 #pragma unroll
-      for (int u = 0; u < PAIR; ++u)
-        if (ok[u]) {
-          // rows outside [lo, L) may hold anything: only retained rows count
-          const int p0 = pos0 + u * TILE + lg, p1 = p0 + 8;
-          if (whole || (p0 >= lo && p0 < L)) et = max(et, f32_exp(vsr[u][0]));
-          if (whole || (p1 >= lo && p1 < L)) et = max(et, f32_exp(vsr[u][1]));
+      for (int c = 0; c < 2; ++c) {
+        float mt = lmax[c];
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+        const float mn = fmaxf(m_run[c], mt);
+        al[c] = (mn == -INFINITY) ? 1.f : ex2(m_run[c] - mn);   // 0 while m_run is -inf
+        l_run[c] *= al[c];
+        m_run[c] = mn;
+      }
+      if constexpr (C::DYN) {
+        int et = et_loc;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) et = max(et, __shfl_xor_sync(0xffffffffu, et, o));
+        const int vnew = max(vexp, max(et, -100));
+        if (vnew != vexp) {
+          const float vfix = pow2i(vexp - vnew);     // 0 on the first tile (O is 0)
+          al[0] *= vfix;
+          al[1] *= vfix;
+          vexp = vnew;
+          fv = pow2i(KP - vexp);
         }
+      }
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) et = max(et, __shfl_xor_sync(0xffffffffu, et, o));
-      const int vnew = max(vexp, max(et, -100));
-      if (vnew != vexp) vfix = pow2i(vexp - vnew);     // 0 on the first tile (acc is 0)
-      vexp = vnew;
-      const float fv = pow2i(13 - vexp);
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < C::MTILES; ++i) {
+          acc[n][i][0] *= al[0];
+          acc[n][i][1] *= al[1];
+          acc[n][i][2] *= al[0];
+          acc[n][i][3] *= al[1];
+        }
+    }
+    float pw[PAIR][4];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      // m_run is -inf only while every score so far is -inf: weights 0
+      const float mu = (m_run[c] == -INFINITY) ? 0.f : m_run[c];
+      float sum = 0.f;
+#pragma unroll
+      for (int u = 0; u < PAIR; ++u) {
+        pw[u][c] = ex2(s_raw[u][c] - mu);
+        pw[u][c + 2] = ex2(s_raw[u][c + 2] - mu);
+        sum += pw[u][c] + pw[u][c + 2];
+      }
+      l_run[c] += sum;
+    }
+    // weights that meet V: P' = p v_scale 2^(KP - vexp) (dynamic), p 2^14 (FP8)
+    if constexpr (C::DYN) {
 #pragma unroll
       for (int u = 0; u < PAIR; ++u) {
         const float f0 = vsr[u][0] * fv, f1 = vsr[u][1] * fv;
@@ -871,43 +929,11 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
         for (int e = 0; e < 4; ++e) pw[u][e] *= 16384.f;
     }
 
-    // ---------------- rescale O when a running max or the range factor moved
-    float al_pv[2] = {alpha[0], alpha[1]};
-    if constexpr (PACKED) {
-      const int srcl = lg * 4 + src_t;
-      const float a0 = __shfl_sync(0xffffffffu, alpha[0], srcl);
-      const float a1 = __shfl_sync(0xffffffffu, alpha[1], srcl);
-      al_pv[0] = a0;
-      al_pv[1] = (G == 1) ? a0 : a1;
-    }
-    al_pv[0] *= vfix;
-    al_pv[1] *= vfix;
-    if (__any_sync(0xffffffffu, al_pv[0] != 1.f || al_pv[1] != 1.f)) {
-#pragma unroll
-      for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int i = 0; i < C::MTILES; ++i) {
-          acc[n][i][0] *= al_pv[0];
-          acc[n][i][1] *= al_pv[1];
-          acc[n][i][2] *= al_pv[0];
-          acc[n][i][3] *= al_pv[1];
-        }
-    }
-
     // ---------------- PV for each sub-tile
 #pragma unroll
     for (int u = 0; u < PAIR; ++u) {
       if (!ok[u]) continue;
-      float pr[4] = {pw[u][0], pw[u][1], pw[u][2], pw[u][3]};
-      if constexpr (PACKED) {
-        const int srcl = lg * 4 + src_t;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pr[e] = __shfl_sync(0xffffffffu, pw[u][e], srcl);
-        if constexpr (G == 1) {     // every column of head 0 reads QK column 0
-          pr[1] = pr[0];
-          pr[3] = pr[2];
-        }
-      }
+      const float pr[4] = {pw[u][0], pw[u][1], pw[u][2], pw[u][3]};
       uint32_t pb[NT][2];
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
@@ -952,8 +978,9 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
       if (u >= cnt) break;
       if (j + u + NS < ntiles) {
         fence_proxy_async();
-        issue(cp);
+        issue(cp, blk_next);
         advance(a, cp);
+        blk_next = block_of(cp);
       }
     }
     j += cnt;
@@ -979,6 +1006,9 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
 // the decode kernel; the others combine the partials of their workers.
 template <int D, int G>
 __global__ void __launch_bounds__(32 * G) merge_kernel(const DecodeArgs a) {
+  // launched as a programmatic dependent of the decode kernel: wait until that
+  // grid has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int item = blockIdx.x;
   const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long P = a.item_tiles[item], n = a.item_tiles[item + 1] - P;
@@ -1117,8 +1147,19 @@ cudaError_t launch3(const DecodeArgs& a, cudaStream_t st) {
   decode_kernel<MODE, D, G><<<ctas, WARPS * 32, smem, st>>>(a, km, vm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.workers <= 1) return e;
-  merge_kernel<D, G><<<a.B * a.Hkv, 32 * G, 0, st>>>(a);
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge grid's launch overlaps the
+  // decode grid's tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.B * a.Hkv));
+  cfg.blockDim = dim3(32 * G);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D, G>, a);
 }
 
 template <int MODE, int D, int G>
