@@ -502,6 +502,67 @@ __device__ long long scan_tiles(const DecodeArgs& a, long long find, Cursor* cur
   return base;
 }
 
+// Total tiles T, this warp's share [my0, my1) and the cursor at my0.  For
+// B <= 128 one round of context-length loads (four sequences per lane) serves
+// both; larger batches scan twice.  Returns the share's tile count.
+__device__ int locate(const DecodeArgs& a, int wid, Cursor* cur, int lane) {
+  long long T, my0, my1;
+  if (a.B > 128) {
+    T = scan_tiles(a, -1, cur, lane);
+    my0 = (long long)wid * T / a.workers;
+    my1 = (long long)(wid + 1) * T / a.workers;
+    if (my1 <= my0) return 0;
+    scan_tiles(a, my0, cur, lane);
+    return (int)(my1 - my0);
+  }
+  int n[4], t0[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int b = 32 * i + lane;
+    n[i] = t0[i] = 0;
+    if (b < a.B) {
+      if (a.context_lens[b] < 0) atomicOr(a.err, ERR_BAD_INDEX);
+      n[i] = seq_tiles(a, b, &t0[i]);
+    }
+  }
+  long long incl[4], base[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) incl[i] = (long long)n[i] * a.Hkv;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const long long v = __shfl_up_sync(0xffffffffu, incl[i], o);
+      if (lane >= o) incl[i] += v;
+    }
+  }
+  base[0] = 0;
+#pragma unroll
+  for (int i = 1; i < 4; ++i) base[i] = base[i - 1] + __shfl_sync(0xffffffffu, incl[i - 1], 31);
+  T = base[3] + __shfl_sync(0xffffffffu, incl[3], 31);
+  my0 = (long long)wid * T / a.workers;
+  my1 = (long long)(wid + 1) * T / a.workers;
+  if (my1 <= my0) return 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const long long excl = incl[i] - (long long)n[i] * a.Hkv;
+    const bool here = n[i] > 0 && my0 >= base[i] + excl && my0 < base[i] + incl[i];
+    const unsigned m = __ballot_sync(0xffffffffu, here);
+    if (m) {
+      const int src = __ffs(m) - 1;
+      const long long off = __shfl_sync(0xffffffffu, my0 - base[i] - excl, src);
+      const int nn = __shfl_sync(0xffffffffu, n[i], src);
+      cur->b = 32 * i + src;
+      cur->n = nn;
+      cur->t0 = __shfl_sync(0xffffffffu, t0[i], src);
+      cur->g = (int)(off / nn);
+      cur->k = (int)(off % nn);
+      break;
+    }
+  }
+  return (int)(my1 - my0);
+}
+
 // Worker 0: item tile offsets P_i (i = b*Hkv + g; P_{B*Hkv} = T) for the
 // merge, and zeros for the output of every sequence with no retained position.
 template <int G, int D>
@@ -582,13 +643,9 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
   // ---- this warp's share of the tile list
   Cursor cc;
   cc.b = cc.g = cc.k = cc.n = cc.t0 = 0;
-  const long long T = scan_tiles(a, -1, &cc, lane);
+  const int ntiles = locate(a, wid, &cc, lane);
   if (wid == 0) publish_items<G, D>(a, lane);
-  const long long my0 = (long long)wid * T / a.workers;
-  const long long my1 = (long long)(wid + 1) * T / a.workers;
-  const int ntiles = (int)(my1 - my0);
   if (ntiles <= 0) return;
-  scan_tiles(a, my0, &cc, lane);
   Cursor cp = cc;                                 // producer cursor, NS tiles ahead
 
   if (lane < NS) mbar_init(&wbars[lane], 1);
@@ -604,7 +661,6 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     const int pos0 = (p.t0 + p.k) * TILE;
     return __ldg(a.block_table + (long long)p.b * a.max_blocks + (pos0 >> a.bs_shift));
   };
-  int blk_next = block_of(cp);
   // Copies of the next tile (cursor p, block id blk) into stage pst.  Cell
   // indices fit in 32 bits (the host refuses caches of 2^31 cells or more).
   auto issue = [&](const Cursor& p, const int blk) {
@@ -637,11 +693,21 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
       valid_mask &= ~(1u << st);
     }
   };
-  for (int j = 0; j < NS && j < ntiles; ++j) {
-    issue(cp, blk_next);
-    advance(a, cp);
-    blk_next = block_of(cp);
+  {
+    // block ids of the first NS tiles in one round of loads while they lie in
+    // the starting item (lane j: tile j)
+    int blk0 = -1;
+    if (lane < NS && cc.k + lane < cc.n)
+      blk0 = __ldg(a.block_table + (long long)cc.b * a.max_blocks +
+                   (((cc.t0 + cc.k + lane) * TILE) >> a.bs_shift));
+    for (int j = 0; j < NS && j < ntiles; ++j) {
+      const int bj = __shfl_sync(0xffffffffu, blk0, j);
+      const bool same = cp.b == cc.b && cp.g == cc.g && cp.k == cc.k + j;
+      issue(cp, same ? bj : block_of(cp));
+      advance(a, cp);
+    }
   }
+  int blk_next = block_of(cp);
 
   float ks_static = 1.f, vs_static = 1.f;
   if constexpr (MODE == FP8_PER_TENSOR) { ks_static = a.k_scale[0]; vs_static = a.v_scale[0]; }
@@ -1003,32 +1069,47 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
 
 // Log-sum-exp merge: one CTA per (sequence, KV head) item, one warp per query
 // head of the group.  Items covered by one worker (or by none) were written by
-// the decode kernel; the others combine the partials of their workers.
+// the decode kernel; the others combine the partials of their workers.  The
+// partial rows of the first PRE workers are loaded together with the (m, l)
+// pairs, so an item split over at most PRE workers costs two dependent rounds
+// of loads after the item offsets.
 template <int D, int G>
 __global__ void __launch_bounds__(32 * G) merge_kernel(const DecodeArgs a) {
   // launched as a programmatic dependent of the decode kernel: wait until that
   // grid has completed and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int PRE = 8;
+  constexpr int DL = D / 32;                            // elements per lane
   const int item = blockIdx.x;
   const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long P = a.item_tiles[item], n = a.item_tiles[item + 1] - P;
-  if (n <= 0) return;
   const long long T = a.item_tiles[(long long)a.B * a.Hkv];
+  if (n <= 0) return;
   const long long W = a.workers;
   const long long w0 = ((P + 1) * W - 1) / T;           // worker owning tile P
   const long long w1 = ((P + n) * W - 1) / T;           // worker owning tile P + n - 1
   if (w0 == w1) return;
   const int b = item / a.Hkv, g = item - b * a.Hkv;
-  float acc[D / 32];
+  // a worker whose share is empty (more workers than tiles) wrote nothing, and
+  // its slot may hold anything: such workers get weight 0 and are selected out
+  auto live_w = [&](long long w) { return w <= w1 && (w * T) / W != ((w + 1) * T) / W; };
+  auto row = [&](long long w) { return a.ws_o + ((item + w) * G + j) * D; };
+  float pre[PRE][DL];
 #pragma unroll
-  for (int k = 0; k < D / 32; ++k) acc[k] = 0.f;
+  for (int u = 0; u < PRE; ++u) {
+    const long long w = (w0 + u <= w1) ? w0 + u : w0;
+#pragma unroll
+    for (int k = 0; k < DL; ++k) pre[u][k] = row(w)[lane + 32 * k];
+  }
+  float acc[DL];
+#pragma unroll
+  for (int k = 0; k < DL; ++k) acc[k] = 0.f;
   float M = -INFINITY, lsum = 0.f;
-  // chunks of 32 workers: lane w-w0 holds that worker's (m, l)
+  // chunks of 32 workers: lane w-c0 holds that worker's (m, l)
   for (long long c0 = w0; c0 <= w1; c0 += 32) {
     const long long w = c0 + lane;
     float m = -INFINITY, l = 0.f;
-    // a worker whose share is empty (more workers than tiles) wrote nothing
-    const bool live = w <= w1 && (w * T) / W != ((w + 1) * T) / W;
+    const bool live = live_w(w);
     const long long part = (item + w) * G + j;
     if (live) {
       m = a.ws_ml[2 * part];
@@ -1045,32 +1126,41 @@ __global__ void __launch_bounds__(32 * G) merge_kernel(const DecodeArgs a) {
     for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
     lsum = lsum * rescale + ls;
 #pragma unroll
-    for (int k = 0; k < D / 32; ++k) acc[k] *= rescale;
+    for (int k = 0; k < DL; ++k) acc[k] *= rescale;
     const int cnt = (int)min(32LL, w1 - c0 + 1);
-    for (int i0 = 0; i0 < cnt; i0 += 4) {
+    int i0 = 0;
+    if (c0 == w0) {
+      // the prefetched rows
+#pragma unroll
+      for (int u = 0; u < PRE; ++u) {
+        const float fu = (u < cnt) ? __shfl_sync(0xffffffffu, f, u) : 0.f;
+#pragma unroll
+        for (int k = 0; k < DL; ++k) acc[k] = fu != 0.f ? fmaf(fu, pre[u][k], acc[k]) : acc[k];
+      }
+      i0 = PRE;
+    }
+    for (; i0 < cnt; i0 += 4) {
       // four partials' loads in flight at once; missing ones read slot c0
-      float v[4][D / 32], fi[4];
+      float v[4][DL], fi[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         fi[u] = __shfl_sync(0xffffffffu, f, (i0 + u) & 31);
         const long long ii = (i0 + u < cnt) ? i0 + u : 0;
         if (i0 + u >= cnt) fi[u] = 0.f;
-        const float* src = a.ws_o + ((item + c0 + ii) * G + j) * D;
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k) v[u][k] = src[lane + 32 * k];
+        for (int k = 0; k < DL; ++k) v[u][k] = row(c0 + ii)[lane + 32 * k];
       }
-      // a slot of an empty or missing share may hold anything: select, not 0 x
 #pragma unroll
       for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k) acc[k] = fi[u] != 0.f ? fmaf(fi[u], v[u][k], acc[k]) : acc[k];
+        for (int k = 0; k < DL; ++k) acc[k] = fi[u] != 0.f ? fmaf(fi[u], v[u][k], acc[k]) : acc[k];
     }
     M = Mn;
   }
   float* out = a.out + ((long long)b * a.Hq + g * G + j) * D;
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
-  for (int k = 0; k < D / 32; ++k) out[lane + 32 * k] = acc[k] * inv;
+  for (int k = 0; k < DL; ++k) out[lane + 32 * k] = acc[k] * inv;
 }
 
 // ------------------------------------------------------------------ host
