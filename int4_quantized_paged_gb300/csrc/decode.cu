@@ -47,15 +47,13 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "async_copy.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {
 namespace {
 
 constexpr int WARPS = 4;         // worker warps per CTA (independent)
-#ifndef KVQ_WAIT_HINT_NS
-#define KVQ_WAIT_HINT_NS 0     // suspend-time hint of one mbarrier try (0: none)
-#endif
 #ifndef KVQ_TILES_PER_ITER
 #define KVQ_TILES_PER_ITER 1
 #endif
@@ -65,63 +63,12 @@ constexpr int WARPS = 4;         // worker warps per CTA (independent)
 constexpr int PAIR = KVQ_TILES_PER_ITER;   // 16-position tiles per loop iteration
 constexpr int TILE = 16;         // positions per tile
 constexpr int KP = 13;           // P' = p v_scale 2^(KP - vexp) < 2^14 (dynamic scales)
-constexpr long long SPIN_LIMIT_CYCLES = 4000000000LL;   // about 2 s at 2 GHz
 
 // ------------------------------------------------------------------ PTX
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// One try.  With a suspend-time hint (ns) the thread may sleep until the
-// phase completes instead of returning at once.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-#if KVQ_WAIT_HINT_NS > 0
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
-      "selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)KVQ_WAIT_HINT_NS)
-      : "memory");
-#else
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
-      "selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-#endif
-  return ok != 0;
-}
-
-// Bounded wait; returns false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > SPIN_LIMIT_CYCLES) return false;
-  }
-  return true;
 }
 
 __device__ __forceinline__ void tma_tile_2d(void* dst, const CUtensorMap* map, int x, int y,
@@ -131,19 +78,6 @@ __device__ __forceinline__ void tma_tile_2d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
-}
-
-__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Four E4M3 codes (one word) -> two f16x2: bytes 0,1 -> lo; bytes 2,3 -> hi.
@@ -649,7 +583,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
   Cursor cp = cc;                                 // producer cursor, NS tiles ahead
 
   if (lane < NS) mbar_init(&wbars[lane], 1);
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  mbar_init_fence();
   __syncwarp();
 
   unsigned valid_mask = 0;        // bit s: stage s holds a fetched tile

@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "async_copy.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -63,6 +64,75 @@ __device__ __forceinline__ float group_max(float v) {
   return v;
 }
 
+// Unpacks 8 bf16 (one 16-byte word group) to fp32.
+__device__ __forceinline__ void unpack8(float* x, const uint4 raw) {
+  x[0] = bf16_lo(raw.x); x[1] = bf16_hi(raw.x);
+  x[2] = bf16_lo(raw.y); x[3] = bf16_hi(raw.y);
+  x[4] = bf16_lo(raw.z); x[5] = bf16_hi(raw.z);
+  x[6] = bf16_lo(raw.w); x[7] = bf16_hi(raw.w);
+}
+
+// Dynamic scale from the vector's amax: s = RN32(amax / qmax), 1.0 for a zero
+// vector.  Computed by the reciprocal correction below (exact for every bf16
+// amax >= 2^-100); IEEE division under that.
+template <int MODE>
+__device__ __forceinline__ float dynamic_scale(float m) {
+  constexpr float qmax = (MODE == INT4_PER_TOKEN_HEAD) ? 7.0f : 448.0f;
+  constexpr float rq = 1.0f / qmax;                         // RN(1/qmax)
+  if (m >= 0x1p-100f) {
+    const float q0 = __fmul_rn(m, rq);
+    return __fmaf_rn(__fmaf_rn(-q0, qmax, m), rq, q0);
+  }
+  return (m == 0.f) ? 1.0f : __fdiv_rn(m, qmax);
+}
+
+// y = RN32(x / s).  One correctly rounded reciprocal per vector, then per
+// element q0 = RN(x r) and the FMA correction q1 = RN(q0 + RN(x - q0 s) r),
+// which is the correctly rounded quotient while the remainder x - q0 s is
+// exact (Markstein's theorem: r within half an ulp of 1/s, q0 within an ulp).
+// That holds away from fp32 underflow; below the guard the kernel divides.
+// Verified equal to IEEE division over every dynamic scale (every bf16 amax,
+// /448 and /7, every bf16 |x| <= amax) where the result decides a code, and
+// over random static scales.  With a static scale the quotient can be huge;
+// past 1e30 it saturates either way, so the correction is skipped there.
+// With a dynamic scale |x/s| <= qmax (1 + 2^-23), so no guard is needed.
+template <int MODE, int N>
+__device__ __forceinline__ void divide_rn(float* y, const float* x, float s) {
+  constexpr bool DYN = (MODE == FP8_PER_TOKEN_HEAD || MODE == INT4_PER_TOKEN_HEAD);
+  constexpr float kLo = DYN ? 0x1p-100f : 0x1p-60f;
+  if (s >= kLo && s <= 0x1p100f) {
+    const float r = __frcp_rn(s);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const float q0 = __fmul_rn(x[i], r);
+      const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, x[i]), r, q0);
+      y[i] = (DYN || fabsf(q0) < 1e30f) ? q1 : q0;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) y[i] = __fdiv_rn(x[i], s);
+  }
+}
+
+// Codes of N quotients: E4M3 bytes (N/4 words) or packed INT4 nibbles, even
+// element in the low nibble (N/8 words).
+template <int MODE, int N>
+__device__ __forceinline__ void encode(uint32_t* w, const float* y) {
+  if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
+#pragma unroll
+    for (int k = 0; k < N / 8; ++k) {
+      uint32_t packed = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) packed |= int4_code(y[8 * k + i]) << (4 * i);
+      w[k] = packed;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < N / 4; ++k)
+      w[k] = e4m3x2(y[4 * k], y[4 * k + 1]) | (e4m3x2(y[4 * k + 2], y[4 * k + 3]) << 16);
+  }
+}
+
 // Quantize and store one vector's 8-element slice held by this lane.
 template <int MODE, int D>
 __device__ __forceinline__ void quantize_store(const WriteArgs& a, const uint4 raw, int is_v, int h,
@@ -73,10 +143,7 @@ __device__ __forceinline__ void quantize_store(const WriteArgs& a, const uint4 r
     reinterpret_cast<uint4*>(cache + cell * (2 * D))[sub] = raw;
   } else {
     float x[8];
-    x[0] = bf16_lo(raw.x); x[1] = bf16_hi(raw.x);
-    x[2] = bf16_lo(raw.y); x[3] = bf16_hi(raw.y);
-    x[4] = bf16_lo(raw.z); x[5] = bf16_hi(raw.z);
-    x[6] = bf16_lo(raw.w); x[7] = bf16_hi(raw.w);
+    unpack8(x, raw);
     float s;
     if constexpr (MODE == FP8_PER_TENSOR) {
       s = __ldg(is_v ? a.v_scale : a.k_scale);
@@ -86,55 +153,17 @@ __device__ __forceinline__ void quantize_store(const WriteArgs& a, const uint4 r
       float m = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
-      m = group_max<LPV>(m);
-      constexpr float qmax = (MODE == INT4_PER_TOKEN_HEAD) ? 7.0f : 448.0f;
-      // s = RN32(amax / qmax) by the same reciprocal correction as below
-      // (exact for every bf16 amax >= 2^-100); IEEE division under that.
-      constexpr float rq = 1.0f / qmax;                         // RN(1/qmax)
-      if (m >= 0x1p-100f) {
-        const float q0 = __fmul_rn(m, rq);
-        s = __fmaf_rn(__fmaf_rn(-q0, qmax, m), rq, q0);
-      } else {
-        s = (m == 0.f) ? 1.0f : __fdiv_rn(m, qmax);
-      }
+      s = dynamic_scale<MODE>(group_max<LPV>(m));
       if (sub == 0) (is_v ? a.v_cs : a.k_cs)[cell] = s;
     }
-    // y = RN32(x / s).  One correctly rounded reciprocal per vector, then per
-    // element q0 = RN(x r) and the FMA correction q1 = RN(q0 + RN(x - q0 s) r),
-    // which is the correctly rounded quotient while the remainder x - q0 s
-    // is exact (Markstein's theorem: r within half an ulp of 1/s, q0 within
-    // an ulp).  That holds away from fp32 underflow; below the guard the
-    // kernel divides.  Verified equal to IEEE division over every dynamic
-    // scale (every bf16 amax, /448 and /7, every bf16 |x| <= amax) where
-    // the result decides a code, and over random static scales.  With a
-    // static scale the quotient can be huge; past 1e30 it saturates either
-    // way, so the correction is skipped there.  With a dynamic scale
-    // |x/s| <= qmax (1 + 2^-23), so no guard is needed.
-    constexpr bool DYN = (MODE == FP8_PER_TOKEN_HEAD || MODE == INT4_PER_TOKEN_HEAD);
     float y[8];
-    constexpr float kLo = DYN ? 0x1p-100f : 0x1p-60f;
-    if (s >= kLo && s <= 0x1p100f) {
-      const float r = __frcp_rn(s);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float q0 = __fmul_rn(x[i], r);
-        const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, x[i]), r, q0);
-        y[i] = (DYN || fabsf(q0) < 1e30f) ? q1 : q0;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(x[i], s);
-    }
+    divide_rn<MODE, 8>(y, x, s);
+    uint32_t w[2];
+    encode<MODE, 8>(w, y);
     if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
-      uint32_t packed = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) packed |= int4_code(y[i]) << (4 * i);
-      reinterpret_cast<uint32_t*>(cache + cell * (D / 2))[sub] = packed;
+      reinterpret_cast<uint32_t*>(cache + cell * (D / 2))[sub] = w[0];
     } else {
-      uint2 o;
-      o.x = e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16);
-      o.y = e4m3x2(y[4], y[5]) | (e4m3x2(y[6], y[7]) << 16);
-      reinterpret_cast<uint2*>(cache + cell * D)[sub] = o;
+      reinterpret_cast<uint2*>(cache + cell * D)[sub] = make_uint2(w[0], w[1]);
     }
   }
 }
@@ -193,21 +222,215 @@ __global__ void __launch_bounds__(256) write_kernel(WriteArgs a) {
   }
 }
 
-template <int MODE>
-cudaError_t launch_mode(int D, const WriteArgs& a, cudaStream_t st) {
+// Staged write for large token counts.  Each CTA takes chunks of TT tokens
+// (chunk c, c + grid, ...) and streams their K and V rows (one bulk copy per
+// token row) through a WNS-stage shared-memory ring; bytes in flight no
+// longer depend on registers.  One group of D/16 lanes quantizes one head
+// vector, 16 elements per lane.  The arithmetic is that of write_kernel.
+constexpr int WNS = 3;            // ring stages
+constexpr int WTHREADS = 256;
+constexpr int WMAXTT = 32;        // tokens per chunk at most
+
+struct StagedLayout {
+  unsigned row;                   // bytes of one token's K (or V) row: Hkv * D * 2
+  int tt;                         // tokens per chunk
+  unsigned stage;                 // 2 * tt * row
+  unsigned smem;                  // ring + slot table + barriers
+};
+
+__host__ __device__ inline StagedLayout staged_layout(int Hkv, int D) {
+  StagedLayout l;
+  l.row = (unsigned)Hkv * D * 2;
+  int tt = (int)(8192u / l.row);    // about 16 KB of K and V rows per stage
+  l.tt = tt < 1 ? 1 : (tt > WMAXTT ? WMAXTT : tt);
+  l.stage = 2u * l.tt * l.row;
+  l.smem = WNS * l.stage + WNS * WMAXTT * 8 + WNS * 8;
+  return l;
+}
+
+template <int MODE, int D>
+__global__ void __launch_bounds__(WTHREADS, 4) write_staged_kernel(const WriteArgs a) {
+  constexpr int LPV = D / 16;                 // lanes per vector
+  constexpr int GROUPS = WTHREADS / LPV;
+  constexpr int RB = (MODE == BF16) ? 2 * D : (MODE == INT4_PER_TOKEN_HEAD ? D / 2 : D);
+  constexpr bool DYN = (MODE == FP8_PER_TOKEN_HEAD || MODE == INT4_PER_TOKEN_HEAD);
+  extern __shared__ __align__(128) uint8_t smem[];
+  const StagedLayout ly = staged_layout(a.Hkv, D);
+  const int TT = ly.tt;
+  long long* slot_s = reinterpret_cast<long long*>(smem + WNS * ly.stage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WNS * ly.stage + WNS * WMAXTT * 8);
+  const int tid = threadIdx.x;
+  const int grp = tid / LPV, sub = tid % LPV;
+  const long long nchunks = (a.T + TT - 1) / TT;
+  if ((long long)blockIdx.x >= nchunks) return;     // whole CTA: before any barrier
+  if (tid == 0) {
+    for (int s = 0; s < WNS; ++s) mbar_init(&bars[s], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  // thread 0: chunk c's rows into stage st
+  auto issue = [&](long long c, int st) {
+    const long long t0 = c * TT;
+    const int nt = (int)min((long long)TT, a.T - t0);
+    uint8_t* dst = smem + st * ly.stage;
+    mbar_expect_tx(&bars[st], 2u * nt * ly.row);
+    for (int i = 0; i < nt; ++i) {
+      const long long src = (t0 + i) * a.token_stride;
+      bulk_copy(dst + i * ly.row, a.k_new + src, ly.row, &bars[st]);
+      bulk_copy(dst + (TT + i) * ly.row, a.v_new + src, ly.row, &bars[st]);
+    }
+  };
+  if (tid == 0)
+    for (int k = 0; k < WNS; ++k) {
+      const long long c = blockIdx.x + (long long)k * gridDim.x;
+      if (c < nchunks) issue(c, k);
+    }
+
+  const long long cells = a.num_blocks * a.bs;      // < 2^31 (checked on the host)
+  const unsigned hkv = (unsigned)a.Hkv;
+  // r / Hkv as a multiply-high: exact for r < 2^32 / Hkv, and r < 64 Hkv here
+  const unsigned long long magic = ((1ull << 32) + hkv - 1) / hkv;
+  int st = 0;
+  uint32_t par = 0;
+  for (long long c = blockIdx.x; c < nchunks; c += gridDim.x) {
+    const long long t0 = c * TT;
+    const int nt = (int)min((long long)TT, a.T - t0);
+    // the chunk's slots, loaded while its rows are in flight
+    const long long my_slot = tid < nt ? __ldg(a.slots + t0 + tid) : -1;
+    const bool ok = mbar_wait(&bars[st], par);
+    if (tid < nt) slot_s[st * WMAXTT + tid] = my_slot;
+    if (__syncthreads_or(!ok)) {
+      // a copy never completed: flag it, let the other stages' copies land
+      // (bounded), and stop
+      if (tid == 0) {
+        atomicOr(a.err, ERR_TIMEOUT);
+        int s2 = st;
+        uint32_t p2 = par;
+        for (int k = 1; k < WNS; ++k) {
+          if (++s2 == WNS) { s2 = 0; p2 ^= 1u; }
+          if (c + (long long)k * gridDim.x < nchunks) (void)mbar_wait(&bars[s2], p2);
+        }
+      }
+      return;
+    }
+    const uint8_t* rows = smem + st * ly.stage;
+    const int nvec = nt * a.Hkv;                       // vectors per tensor in the chunk
+    for (int v = grp; v < 2 * nvec; v += GROUPS) {
+      const int is_v = v >= nvec;
+      const int r = is_v ? v - nvec : v;
+      const unsigned i = (unsigned)(((unsigned long long)(unsigned)r * magic) >> 32);
+      const unsigned h = (unsigned)r - i * hkv;
+      const long long slot = slot_s[st * WMAXTT + i];
+      if (slot < 0) continue;                          // whole group agrees
+      if (slot >= cells) {
+        if (sub == 0 && !is_v && h == 0) atomicOr(a.err, ERR_BAD_INDEX);
+        continue;
+      }
+      const unsigned sl = (unsigned)slot;
+      const unsigned cell = (((sl >> a.bs_shift) * hkv + h) << a.bs_shift) | (sl & (a.bs - 1));
+      const uint8_t* src = rows + (is_v ? TT + i : i) * ly.row + h * (2 * D) + sub * 32;
+      const uint4 r0 = *reinterpret_cast<const uint4*>(src);
+      const uint4 r1 = *reinterpret_cast<const uint4*>(src + 16);
+      uint8_t* dst = (is_v ? a.v_cache : a.k_cache) + (size_t)cell * RB;
+      if constexpr (MODE == BF16) {
+        reinterpret_cast<uint4*>(dst)[2 * sub] = r0;
+        reinterpret_cast<uint4*>(dst)[2 * sub + 1] = r1;
+      } else {
+        float x[16];
+        unpack8(x, r0);
+        unpack8(x + 8, r1);
+        float s;
+        if constexpr (MODE == FP8_PER_TENSOR) {
+          s = __ldg(is_v ? a.v_scale : a.k_scale);
+        } else if constexpr (MODE == FP8_PER_HEAD) {
+          s = __ldg((is_v ? a.v_scale : a.k_scale) + h);
+        } else {
+          float m = 0.f;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(x[e]));
+          s = dynamic_scale<MODE>(group_max<LPV>(m));
+          if (sub == 0) (is_v ? a.v_cs : a.k_cs)[cell] = s;
+        }
+        float y[16];
+        divide_rn<MODE, 16>(y, x, s);
+        uint32_t w[4];
+        encode<MODE, 16>(w, y);
+        if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
+          reinterpret_cast<uint2*>(dst)[sub] = make_uint2(w[0], w[1]);
+        } else {
+          reinterpret_cast<uint4*>(dst)[sub] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    (void)DYN;
+    __syncthreads();                                   // stage st fully read
+    if (tid == 0) {
+      const long long cn = c + (long long)WNS * gridDim.x;
+      if (cn < nchunks) {
+        fence_proxy_async();
+        issue(cn, st);
+      }
+    }
+    if (++st == WNS) { st = 0; par ^= 1u; }
+  }
+}
+
+// Resident staged-write CTAs per SM for this layout (0: not launchable).
+template <int MODE, int D>
+int staged_ctas_per_sm(unsigned smem) {
+  static int max_set[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  auto kern = write_staged_kernel<MODE, D>;
+  if (!max_set[dev]) {
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+            cudaSuccess)
+      return 0;
+    max_set[dev] = optin;
+  }
+  if ((int)smem > max_set[dev]) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, WTHREADS, smem) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <int MODE, int D>
+cudaError_t launch_write_d(const WriteArgs& a, cudaStream_t st) {
+  // staged path once there is at least one chunk per SM
+  const StagedLayout ly = staged_layout(a.Hkv, D);
+  const long long nchunks = (a.T + ly.tt - 1) / ly.tt;
+  if (nchunks >= sm_count()) {
+    const int per_sm = staged_ctas_per_sm<MODE, D>(ly.smem);
+    if (per_sm > 0) {
+      long long grid = (long long)sm_count() * per_sm;
+      if (grid > nchunks) grid = nchunks;
+      write_staged_kernel<MODE, D><<<(unsigned)grid, WTHREADS, ly.smem, st>>>(a);
+      return cudaGetLastError();
+    }
+  }
   const long long lanes_needed = 2 * a.T * a.Hkv * (D / 8);
   const int threads = 256;
   long long blocks = (lanes_needed + threads - 1) / threads;
   const long long cap = (long long)sm_count() * 8 * 4;      // resident blocks x 4; grid-stride beyond
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  write_kernel<MODE, D><<<(unsigned)blocks, threads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_mode(int D, const WriteArgs& a, cudaStream_t st) {
   switch (D) {
-    case 64: write_kernel<MODE, 64><<<(unsigned)blocks, threads, 0, st>>>(a); break;
-    case 128: write_kernel<MODE, 128><<<(unsigned)blocks, threads, 0, st>>>(a); break;
-    case 256: write_kernel<MODE, 256><<<(unsigned)blocks, threads, 0, st>>>(a); break;
+    case 64: return launch_write_d<MODE, 64>(a, st);
+    case 128: return launch_write_d<MODE, 128>(a, st);
+    case 256: return launch_write_d<MODE, 256>(a, st);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- calibration

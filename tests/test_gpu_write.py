@@ -34,6 +34,24 @@ def test_write_bit_exact_small(name, mode):
     r.check_write()
 
 
+# Writes of fewer chunks than SMs take the direct kernel (registers hold the
+# rows), larger ones the staged kernel (rows streamed through shared memory);
+# SMALL covers both (tiny and gptoss direct, the others staged).  These add
+# the direct path at D = 128 and 256 in every mode.
+DIRECT = {
+    "llama8b_b1": wl.scaled(wl.CONFIGS["llama8b"], batch=1, context=200),
+    "gemma_b1": wl.scaled(wl.CONFIGS["gemma_d256"], batch=1, context=300),
+}
+
+
+@pytest.mark.parametrize("name", list(DIRECT))
+@pytest.mark.parametrize("mode", MODES)
+def test_write_bit_exact_direct_path(name, mode):
+    r = LayerRun(DIRECT[name], mode)
+    r.write()
+    r.check_write()
+
+
 @pytest.mark.parametrize("mode", [orc.FP8_PER_TENSOR, orc.FP8_PER_HEAD, orc.FP8_PER_TOKEN_HEAD])
 def test_write_bit_exact_llama8b_full_fill(mode):
     r = LayerRun(wl.CONFIGS["llama8b"], mode)
@@ -104,9 +122,32 @@ def test_slot_past_the_cache_is_reported_not_written():
     r.check_write()
 
 
-def test_strided_token_rows():
-    # K and V as column slices of one [T, 3, Hkv*D] projection output.
+def test_slot_past_the_cache_staged_path():
     w = SMALL["llama8b"]
+    r = LayerRun(w, orc.INT4_PER_TOKEN_HEAD)
+    kvq = K()
+    pos = wl.fill_positions(w)
+    T = sum(len(p) for p in pos)
+    k, v = wl.kv_tokens(w, T, "cuda")
+    slots = wl.slot_mapping(w, r.pg, pos, "cuda")
+    cap = r.pg.num_blocks * w.block_size
+    bad = torch.tensor([7, 1500, T - 1], device="cuda")
+    slots[bad] = torch.tensor([cap, cap + 5, 1 << 40], dtype=torch.int64, device="cuda")
+    kvq.kvq_cache_write(r.ctx, 0, k, v, slots, r.kc, r.vc, r.ks, r.vs)
+    assert kvq.kvq_get_device_error() == kvq.STATUS.index("KVQ_ERR_BAD_INDEX")
+    good = slots.cpu().numpy().copy()
+    good[bad.cpu().numpy()] = -1
+    kc, vc, ks, vs = orc.alloc_cache(orc.INT4_PER_TOKEN_HEAD, r.pg.num_blocks, w.Hkv, 16, w.D)
+    orc.cache_write(orc.INT4_PER_TOKEN_HEAD, bits(k), bits(v), good, kc, vc, ks, vs)
+    r.host = (kc, vc, ks, vs)
+    r.check_write()
+
+
+@pytest.mark.parametrize("name", ["llama8b", "tiny"])
+def test_strided_token_rows(name):
+    # K and V as column slices of one [T, 3, Hkv*D] projection output
+    # (llama8b: staged path; tiny: direct path).
+    w = SMALL[name]
     r = LayerRun(w, orc.FP8_PER_TOKEN_HEAD)
     kvq = K()
     pos = wl.fill_positions(w)
