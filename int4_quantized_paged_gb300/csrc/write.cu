@@ -45,12 +45,6 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ uint32_t int4_code(float y) {
-  int q = __float2int_rn(y);              // round to nearest even
-  q = max(-7, min(7, q));
-  return (uint32_t)q & 0xFu;
-}
-
 // Max over the LPV lanes of one vector group.  Groups of one warp may take
 // different paths (a skipped slot, the end of the grid-stride loop), so the
 // shuffle names only the group's own lanes.
@@ -116,15 +110,29 @@ __device__ __forceinline__ void divide_rn(float* y, const float* x, float s) {
 
 // Codes of N quotients: E4M3 bytes (N/4 words) or packed INT4 nibbles, even
 // element in the low nibble (N/8 words).
+//
+// INT4: for |y| < 2^22, RN(y + 1.5 * 2^23) = 1.5 * 2^23 + RNE(y) exactly (the
+// sum's ulp is 1, ties go to the even significand, i.e. to even RNE(y)), and
+// the bit pattern of that float is the pattern of 1.5 * 2^23 (low bits 0)
+// plus RNE(y), so its low four bits are RNE(y) as a two's-complement nibble.
+// The per-token-head scale keeps |y| <= 7 (1 + 2^-23) (s = RN(amax / 7),
+// |x| <= amax, and the scale's rounding error is far below 1/14 down to the
+// smallest bf16 amax), so RNE(y) already lies in [-7, 7] and needs no clamp.
 template <int MODE, int N>
 __device__ __forceinline__ void encode(uint32_t* w, const float* y) {
   if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
+    constexpr float kRound = 12582912.0f;                     // 1.5 * 2^23
 #pragma unroll
     for (int k = 0; k < N / 8; ++k) {
-      uint32_t packed = 0;
+      uint32_t b[4];                                          // byte j in the low 8 bits
 #pragma unroll
-      for (int i = 0; i < 8; ++i) packed |= int4_code(y[8 * k + i]) << (4 * i);
-      w[k] = packed;
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = __float_as_uint(__fadd_rn(y[8 * k + 2 * j], kRound));
+        const uint32_t hi = __float_as_uint(__fadd_rn(y[8 * k + 2 * j + 1], kRound));
+        b[j] = (lo & 0x0Fu) | ((hi << 4) & 0xF0u);
+      }
+      w[k] = __byte_perm(__byte_perm(b[0], b[1], 0x0040u), __byte_perm(b[2], b[3], 0x0040u),
+                         0x5410u);
     }
   } else {
 #pragma unroll
@@ -401,10 +409,11 @@ int staged_ctas_per_sm(unsigned smem) {
 
 template <int MODE, int D>
 cudaError_t launch_write_d(const WriteArgs& a, cudaStream_t st) {
-  // staged path once there is at least one chunk per SM
+  // staged path once there is at least one chunk per SM (a BF16 layer is a
+  // plain copy, which the direct kernel streams faster)
   const StagedLayout ly = staged_layout(a.Hkv, D);
   const long long nchunks = (a.T + ly.tt - 1) / ly.tt;
-  if (nchunks >= sm_count()) {
+  if (MODE != BF16 && nchunks >= sm_count()) {
     const int per_sm = staged_ctas_per_sm<MODE, D>(ly.smem);
     if (per_sm > 0) {
       long long grid = (long long)sm_count() * per_sm;
