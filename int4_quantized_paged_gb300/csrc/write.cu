@@ -231,19 +231,23 @@ __global__ void __launch_bounds__(256) write_kernel(WriteArgs a) {
 }
 
 // Staged write for large token counts.  Each CTA takes chunks of TT tokens
-// (chunk c, c + grid, ...) and streams their K and V rows (one bulk copy per
-// token row) through a WNS-stage shared-memory ring; bytes in flight no
-// longer depend on registers.  One group of D/16 lanes quantizes one head
-// vector, 16 elements per lane.  The arithmetic is that of write_kernel.
+// (chunk c, c + grid, ...).  A producer warp streams the chunks' K and V rows
+// (one bulk copy per token row) and slot indices through a WNS-stage
+// shared-memory ring; eight consumer warps quantize from it, one group of
+// D/16 lanes per head vector, 16 elements per lane, and release each stage on
+// its "empty" barrier, so no warp waits for another except through the ring.
+// Bytes in flight do not depend on registers.  The arithmetic is that of
+// write_kernel.
 constexpr int WNS = 3;            // ring stages
-constexpr int WTHREADS = 256;
+constexpr int WCONSUMERS = 256;   // consumer threads (8 warps)
+constexpr int WTHREADS = WCONSUMERS + 32;
 constexpr int WMAXTT = 32;        // tokens per chunk at most
 
 struct StagedLayout {
   unsigned row;                   // bytes of one token's K (or V) row: Hkv * D * 2
   int tt;                         // tokens per chunk
   unsigned stage;                 // 2 * tt * row
-  unsigned smem;                  // ring + slot table + barriers
+  unsigned smem;                  // ring + slot table + full and empty barriers
 };
 
 __host__ __device__ inline StagedLayout staged_layout(int Hkv, int D) {
@@ -252,49 +256,68 @@ __host__ __device__ inline StagedLayout staged_layout(int Hkv, int D) {
   int tt = (int)(8192u / l.row);    // about 16 KB of K and V rows per stage
   l.tt = tt < 1 ? 1 : (tt > WMAXTT ? WMAXTT : tt);
   l.stage = 2u * l.tt * l.row;
-  l.smem = WNS * l.stage + WNS * WMAXTT * 8 + WNS * 8;
+  l.smem = WNS * l.stage + WNS * WMAXTT * 8 + 2 * WNS * 8;
   return l;
 }
 
 template <int MODE, int D>
 __global__ void __launch_bounds__(WTHREADS, 4) write_staged_kernel(const WriteArgs a) {
   constexpr int LPV = D / 16;                 // lanes per vector
-  constexpr int GROUPS = WTHREADS / LPV;
+  constexpr int GROUPS = WCONSUMERS / LPV;
   constexpr int RB = (MODE == BF16) ? 2 * D : (MODE == INT4_PER_TOKEN_HEAD ? D / 2 : D);
-  constexpr bool DYN = (MODE == FP8_PER_TOKEN_HEAD || MODE == INT4_PER_TOKEN_HEAD);
   extern __shared__ __align__(128) uint8_t smem[];
   const StagedLayout ly = staged_layout(a.Hkv, D);
   const int TT = ly.tt;
   long long* slot_s = reinterpret_cast<long long*>(smem + WNS * ly.stage);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WNS * ly.stage + WNS * WMAXTT * 8);
-  const int tid = threadIdx.x;
-  const int grp = tid / LPV, sub = tid % LPV;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + WNS * ly.stage + WNS * WMAXTT * 8);
+  uint64_t* empty = full + WNS;
+  const int tid = threadIdx.x, lane = tid & 31;
   const long long nchunks = (a.T + TT - 1) / TT;
   if ((long long)blockIdx.x >= nchunks) return;     // whole CTA: before any barrier
   if (tid == 0) {
-    for (int s = 0; s < WNS; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < WNS; ++s) {
+      mbar_init(&full[s], 2);                       // copies' arrive + slots' arrive
+      mbar_init(&empty[s], WCONSUMERS / 32);        // one arrive per consumer warp
+    }
     mbar_init_fence();
   }
-  __syncthreads();
+  __syncthreads();                                  // the only CTA-wide barrier
 
-  // thread 0: chunk c's rows into stage st
-  auto issue = [&](long long c, int st) {
-    const long long t0 = c * TT;
-    const int nt = (int)min((long long)TT, a.T - t0);
-    uint8_t* dst = smem + st * ly.stage;
-    mbar_expect_tx(&bars[st], 2u * nt * ly.row);
-    for (int i = 0; i < nt; ++i) {
-      const long long src = (t0 + i) * a.token_stride;
-      bulk_copy(dst + i * ly.row, a.k_new + src, ly.row, &bars[st]);
-      bulk_copy(dst + (TT + i) * ly.row, a.v_new + src, ly.row, &bars[st]);
+  if (tid >= WCONSUMERS) {
+    // ---------------- producer warp
+    int st = 0;
+    long long k = 0;                                // chunks of this CTA so far
+    for (long long c = blockIdx.x; c < nchunks; c += gridDim.x, ++k) {
+      // the k-th chunk reuses stage k % WNS after the consumers released
+      // chunk k - WNS there: phase k / WNS - 1 of its empty barrier
+      if (k >= WNS && !mbar_wait(&empty[st], (uint32_t)(k / WNS - 1) & 1u)) {
+        if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+        return;
+      }
+      const long long t0 = c * TT;
+      const int nt = (int)min((long long)TT, a.T - t0);
+      uint8_t* dst = smem + st * ly.stage;
+      if (lane == 0) {
+        fence_proxy_async();
+        mbar_expect_tx(&full[st], 2u * nt * ly.row);
+        for (int i = 0; i < nt; ++i) {
+          const long long src = (t0 + i) * a.token_stride;
+          bulk_copy(dst + i * ly.row, a.k_new + src, ly.row, &full[st]);
+          bulk_copy(dst + (TT + i) * ly.row, a.v_new + src, ly.row, &full[st]);
+        }
+      }
+      // the chunk's slots, loaded while its rows are in flight; the arrive
+      // after the warp barrier publishes them with the stage
+      if (lane < nt) slot_s[st * WMAXTT + lane] = __ldg(a.slots + t0 + lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[st]);
+      if (++st == WNS) st = 0;
     }
-  };
-  if (tid == 0)
-    for (int k = 0; k < WNS; ++k) {
-      const long long c = blockIdx.x + (long long)k * gridDim.x;
-      if (c < nchunks) issue(c, k);
-    }
+    return;
+  }
 
+  // ---------------- consumer warps
+  const int grp = tid / LPV, sub = tid % LPV;
   const long long cells = a.num_blocks * a.bs;      // < 2^31 (checked on the host)
   const unsigned hkv = (unsigned)a.Hkv;
   // r / Hkv as a multiply-high: exact for r < 2^32 / Hkv, and r < 64 Hkv here
@@ -304,33 +327,19 @@ __global__ void __launch_bounds__(WTHREADS, 4) write_staged_kernel(const WriteAr
   for (long long c = blockIdx.x; c < nchunks; c += gridDim.x) {
     const long long t0 = c * TT;
     const int nt = (int)min((long long)TT, a.T - t0);
-    // the chunk's slots, loaded while its rows are in flight
-    const long long my_slot = tid < nt ? __ldg(a.slots + t0 + tid) : -1;
-    const bool ok = mbar_wait(&bars[st], par);
-    if (tid < nt) slot_s[st * WMAXTT + tid] = my_slot;
-    if (__syncthreads_or(!ok)) {
-      // a copy never completed: flag it, let the other stages' copies land
-      // (bounded), and stop
-      if (tid == 0) {
-        atomicOr(a.err, ERR_TIMEOUT);
-        int s2 = st;
-        uint32_t p2 = par;
-        for (int k = 1; k < WNS; ++k) {
-          if (++s2 == WNS) { s2 = 0; p2 ^= 1u; }
-          if (c + (long long)k * gridDim.x < nchunks) (void)mbar_wait(&bars[s2], p2);
-        }
-      }
+    if (!mbar_wait(&full[st], par)) {
+      if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
       return;
     }
     const uint8_t* rows = smem + st * ly.stage;
-    const int nvec = nt * a.Hkv;                       // vectors per tensor in the chunk
+    const int nvec = nt * a.Hkv;                     // vectors per tensor in the chunk
     for (int v = grp; v < 2 * nvec; v += GROUPS) {
       const int is_v = v >= nvec;
       const int r = is_v ? v - nvec : v;
       const unsigned i = (unsigned)(((unsigned long long)(unsigned)r * magic) >> 32);
       const unsigned h = (unsigned)r - i * hkv;
       const long long slot = slot_s[st * WMAXTT + i];
-      if (slot < 0) continue;                          // whole group agrees
+      if (slot < 0) continue;                        // whole group agrees
       if (slot >= cells) {
         if (sub == 0 && !is_v && h == 0) atomicOr(a.err, ERR_BAD_INDEX);
         continue;
@@ -371,15 +380,8 @@ __global__ void __launch_bounds__(WTHREADS, 4) write_staged_kernel(const WriteAr
         }
       }
     }
-    (void)DYN;
-    __syncthreads();                                   // stage st fully read
-    if (tid == 0) {
-      const long long cn = c + (long long)WNS * gridDim.x;
-      if (cn < nchunks) {
-        fence_proxy_async();
-        issue(cn, st);
-      }
-    }
+    __syncwarp();                                    // this warp is done with stage st
+    if (lane == 0) mbar_arrive(&empty[st]);
     if (++st == WNS) { st = 0; par ^= 1u; }
   }
 }
