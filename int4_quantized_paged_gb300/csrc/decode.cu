@@ -359,15 +359,13 @@ struct Cfg {
   static constexpr int SCALES = DYN ? 128 : 0;               // K + V scales per stage
   static constexpr int KSTEPS = D / 16;
   static constexpr int MTILES = D / 16;
-  // ring stages per warp: PAIR tiles per iteration plus at least one in
-  // flight; about 13 KB (one tile per iteration) or 18 KB (two) per warp
-  static constexpr int NS0 = (PAIR == 1 ? 13312 : 18432) / STAGE;
-  static constexpr int NSMIN = PAIR + 1;
-#ifdef KVQ_NS
-  static constexpr int NS = KVQ_NS < NSMIN ? NSMIN : KVQ_NS;
-#else
-  static constexpr int NS = NS0 < NSMIN ? NSMIN : (NS0 > 6 ? 6 : NS0);
-#endif
+};
+
+// Resident CTAs per SM the register budget is sized for: four (16 warps,
+// <= 128 registers) where the accumulators fit without spilling, else two.
+template <int MODE, int D, int G>
+struct MinCtas {
+  static constexpr int value = (D == 256 || (G == 8 && D >= 128) || (MODE == BF16 && G >= 4)) ? 2 : 4;
 };
 
 // Shared memory: the warps' rings first (1024-aligned stages for the
@@ -375,11 +373,25 @@ struct Cfg {
 template <int MODE, int D, int G>
 struct Layout {
   using C = Cfg<MODE, D>;
-  static constexpr int ring = C::NS * C::STAGE;
-  static constexpr int scales = C::NS * C::SCALES;
   static constexpr int q = G * D * 2;
-  static constexpr int bars = C::NS * 8;
-  static constexpr int aux = (scales + q + bars + 127) / 128 * 128;
+  static constexpr int aux_of(int ns) { return (ns * C::SCALES + q + ns * 8 + 127) / 128 * 128; }
+  static constexpr int warp_bytes(int ns) { return ns * C::STAGE + aux_of(ns); }
+  // Ring depth: the most stages (at most 6, at least PAIR + 1) with which
+  // MinCtas CTAs share the SM's 228 KB (1 KB per CTA is reserved by the
+  // system, 1 KB of each CTA's is alignment slack).
+  static constexpr int budget = 233472 / MinCtas<MODE, D, G>::value - 2048;
+  static constexpr int fit(int ns) {
+    return (ns > PAIR + 1 && WARPS * warp_bytes(ns) > budget) ? fit(ns - 1) : ns;
+  }
+#ifdef KVQ_NS
+  static constexpr int NS = KVQ_NS < PAIR + 1 ? PAIR + 1 : KVQ_NS;
+#else
+  static constexpr int NS = fit(6);
+#endif
+  static constexpr int ring = NS * C::STAGE;
+  static constexpr int scales = NS * C::SCALES;
+  static constexpr int bars = NS * 8;
+  static constexpr int aux = aux_of(NS);
   static constexpr int total = WARPS * (ring + aux) + 1024;   // + alignment slack
 };
 
@@ -537,20 +549,13 @@ __device__ __forceinline__ void advance(const DecodeArgs& a, Cursor& c) {
   } while (c.n == 0);
 }
 
-// Resident CTAs per SM the register budget is sized for: four (16 warps,
-// <= 128 registers) where the accumulators fit without spilling, else fewer.
-template <int MODE, int D, int G>
-struct MinCtas {
-  static constexpr int value = (D == 256 || G == 8 || (MODE == BF16 && G >= 4)) ? 2 : 4;
-};
-
 template <int MODE, int D, int G>
 __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap) {
   using C = Cfg<MODE, D>;
   using LY = Layout<MODE, D, G>;
-  constexpr int NS = C::NS;
+  constexpr int NS = LY::NS;
   constexpr int NPART = C::BF ? 3 : 2;                       // terms of the P' split
   constexpr bool PACKED = G * NPART <= 8;                    // all terms in one PV tile
   constexpr int NT = PACKED ? 1 : NPART;                     // PV column tiles
