@@ -211,14 +211,14 @@ def layer_modes(w, mode: int, skip_sliding: bool):
     return [0 if (skip_sliding and win > 0) else mode for win in w.windows]
 
 
-def setup_gpu(args, dev, rank):
+def setup_gpu(args, dev, rank, w=None, time_fill=True):
     """Caches of every layer filled with the context minus the current token,
     the step's inputs, workspaces.  Returns a dict of state."""
     import torch
     from int4_quantized_paged_gb300 import kvq
     from int4_quantized_paged_gb300 import workloads as wl
 
-    w = rank_workload(args.workload, rank)
+    w = rank_workload(args.workload, rank) if w is None else w
     L = w.context_lens[0]
     modes = layer_modes(w, kvq.MODE_NAMES[args.mode], args.skip_sliding)
     pg = wl.paging(w, dev)
@@ -249,7 +249,7 @@ def setup_gpu(args, dev, rank):
             kvq.kvq_cache_write(ctx, li, k_all, v_all, slots_all, kc, vc, ks, vs, k_scale, v_scale)
 
         fill()
-        if fill_ms is None and win == 0:
+        if time_fill and fill_ms is None and win == 0:
             # prefill-shaped write of the whole context of one full layer
             for _ in range(3):
                 fill()
@@ -606,6 +606,89 @@ def run_reference(args):
     }
 
 
+def run_latency_sweep(args):
+    """Decode-step latency against context length for BF16, all-FP8, FP8 with
+    BF16 window layers, and INT4 caches on one workload shape (batch fixed),
+    with a least-squares line per variant (intercept, ms per context token)
+    and the context at which each quantized variant breaks even with BF16.
+    Each point is the median of CUDA-graph replays of the whole step (every
+    layer: write of the current token, then decode)."""
+    import types
+    import torch
+    from int4_quantized_paged_gb300 import workloads as wl
+
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    base = wl.CONFIGS[args.workload]
+    contexts = [int(c) for c in args.sweep_contexts.split(",")]
+    variants = [("bf16", "bf16", False), ("fp8", "fp8_per_token_head", False),
+                ("fp8+bf16_sliding", "fp8_per_token_head", True),
+                ("int4", "int4_per_token_head", False)]
+    if not any(win > 0 for win in base.windows):
+        variants = [v for v in variants if not v[2]]
+    points = {name: [] for name, _, _ in variants}
+    stream = torch.cuda.current_stream()
+    for L in contexts:
+        w = wl.scaled(base, context=L)
+        for name, mode, skip in variants:
+            a = types.SimpleNamespace(**{**vars(args), "mode": mode, "skip_sliding": skip})
+            st = setup_gpu(a, dev, 0, w=w, time_fill=False)
+            nl = len(st["layers"])
+
+            def step():
+                for li in range(nl):
+                    launch_layer(st, li)
+
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            s2 = torch.cuda.Stream()
+            s2.wait_stream(stream)
+            with torch.cuda.stream(s2):
+                step()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(graph, stream=s2):
+                    step()
+            torch.cuda.synchronize()
+            reps = 10
+            ts = []
+            for _ in range(7):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    graph.replay()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1) / reps)
+            points[name].append((L, statistics.median(ts)))
+            del st, graph
+            torch.cuda.empty_cache()
+
+    def fit(pts):
+        n = len(pts)
+        mx = sum(x for x, _ in pts) / n
+        my = sum(y for _, y in pts) / n
+        sxx = sum((x - mx) ** 2 for x, _ in pts)
+        b = sum((x - mx) * (y - my) for x, y in pts) / sxx if sxx > 0 else 0.0
+        return my - b * mx, b
+
+    lines = {name: fit(p) for name, p in points.items()}
+    a0, b0 = lines["bf16"]
+    res = {"metric": "decode-step latency vs context (fitted ms per context token; break-even "
+                     "context vs BF16)",
+           "workload": WORKLOADS[args.workload], "batch": base.B, "contexts": contexts,
+           "unit": "ms per step", "variants": {}}
+    for name, (a, b) in lines.items():
+        v = {"ms": [round(y, 4) for _, y in points[name]], "intercept_ms": round(a, 5),
+             "slope_ms_per_token": float("%.4g" % b)}
+        if name != "bf16":
+            v["break_even_context"] = (round((a - a0) / (b0 - b), 1) if b0 != b else None)
+        res["variants"][name] = v
+    return res
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -625,9 +708,16 @@ def main(argv=None):
     ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--cpu-seqs", type=int, default=0, help="0: the workload's default sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--latency-sweep", action="store_true",
+                    help="latency against context for BF16 / FP8 / FP8 + BF16 window layers / "
+                         "INT4 instead of the throughput line")
+    ap.add_argument("--sweep-contexts", default="1024,2048,4096,8192,16384,32768")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
-    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.latency_sweep:
+        res = run_latency_sweep(args)
+    else:
+        res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 
