@@ -88,11 +88,20 @@ __device__ __forceinline__ void e4m3x4_f16(uint32_t w, uint32_t& lo, uint32_t& h
       : "r"(w));
 }
 
-// Two nibble values placed at bits 0-3 and 16-19, offset binary (n ^ 8) ->
-// f16x2 of the signed values (exact): f16(1024 + m) - 1032.
+// The two's-complement nibbles at bits 4P..4P+3 and 16+4P..19+4P of x (P = 0
+// or 1) -> f16x2 of 16^P times their signed values, exactly.  Flipping bit 3
+// of a nibble makes it offset binary m = n + 8; placed in the mantissa under
+// the exponent of 1024 it reads 1024 + 16^P m, and subtracting 1024 + 8 16^P
+// leaves 16^P n.  The flip, the mask and the exponent bits are one
+// three-input logic operation.
+template <int P>
 __device__ __forceinline__ uint32_t nib2_f16x2(uint32_t x) {
-  uint32_t h = (x & 0x000F000Fu) | 0x64006400u, r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64086408u));
+  constexpr uint32_t M = 0x000F000Fu << (4 * P);
+  constexpr uint32_t C = (0x00080008u << (4 * P)) | 0x64006400u;
+  constexpr uint32_t S = P == 0 ? 0x64086408u : 0x64806480u;   // f16 1032 / 1152
+  const uint32_t h = (x & M) ^ C;
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(S));
   return r;
 }
 
@@ -262,10 +271,12 @@ __device__ __forceinline__ void qk_tile(float sacc_out[4], const uint8_t* kt, in
     load_seg<SEGB>(w1, kt, r1 * RB + lt * SEGB, true);
 #pragma unroll
     for (int s = 0; s < KSTEPS; ++s) {
-      const int sh = 8 * (s & 1);
-      const uint32_t x0 = w0[s >> 1] ^ 0x88888888u, x1 = w1[s >> 1] ^ 0x88888888u;
-      const uint32_t af[4] = {nib2_f16x2(x0 >> sh), nib2_f16x2(x1 >> sh),
-                              nib2_f16x2(x0 >> (sh + 4)), nib2_f16x2(x1 >> (sh + 4))};
+      // k-slots 0, 1: nibbles 2(s&1) and 4 + 2(s&1) of the word; k-slots 2, 3:
+      // the next ones, read 16x (q carries the 1/16 for them)
+      const uint32_t x0 = (s & 1) ? (w0[s >> 1] >> 8) : w0[s >> 1];
+      const uint32_t x1 = (s & 1) ? (w1[s >> 1] >> 8) : w1[s >> 1];
+      const uint32_t af[4] = {nib2_f16x2<0>(x0), nib2_f16x2<0>(x1), nib2_f16x2<1>(x0),
+                              nib2_f16x2<1>(x1)};
       mma16816<false>(sacc2[s % NCH], af, qf[s][0], qf[s][1]);
     }
   } else {
@@ -326,15 +337,17 @@ __device__ __forceinline__ void pv_tile(float (*acc)[D / 16][4], const uint8_t* 
       af[2] = __byte_perm(wc[i], wd[i], 0x5410);
       af[3] = __byte_perm(wc[i], wd[i], 0x7632);
     } else if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
-      // byte i of the segment: low nibble = d 2i, high nibble = d 2i+1
+      // byte i of the segment: low nibble = d 2i, high nibble = d 2i+1; the
+      // high nibbles (rows lg + 8: odd d) are read 16x and scaled back in
+      // the epilogue
       const int wi = i >> 2, k = i & 3;
       const uint32_t sel = (uint32_t)(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
-      const uint32_t x = __byte_perm(wa[wi], wb[wi], sel) ^ 0x00880088u;
-      const uint32_t y = __byte_perm(wc[wi], wd[wi], sel) ^ 0x00880088u;
-      af[0] = nib2_f16x2(x);
-      af[1] = nib2_f16x2(x >> 4);
-      af[2] = nib2_f16x2(y);
-      af[3] = nib2_f16x2(y >> 4);
+      const uint32_t x = __byte_perm(wa[wi], wb[wi], sel);
+      const uint32_t y = __byte_perm(wc[wi], wd[wi], sel);
+      af[0] = nib2_f16x2<0>(x);
+      af[1] = nib2_f16x2<1>(x);
+      af[2] = nib2_f16x2<0>(y);
+      af[3] = nib2_f16x2<1>(y);
     } else {
       // bytes 2i, 2i+1 of each position's segment
       const int wi = i >> 1;
@@ -717,10 +730,12 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
         const float f = full ? (l > 0.f ? unscale / l : 0.f) : unscale;
         float* dst = full ? a.out + (((long long)seg_b * a.Hq + seg_g * G + h) * D)
                           : a.ws_o + (((long long)(item + wid) * G + h) * D);
+        // INT4: the odd-d rows were accumulated 16x (see pv_tile)
+        const float f_odd = (MODE == INT4_PER_TOKEN_HEAD) ? f * 0.0625f : f;
 #pragma unroll
         for (int i = 0; i < C::MTILES; ++i) {
           const int d = lg * (D / 8) + 2 * i;
-          *reinterpret_cast<float2*>(dst + d) = make_float2(o[i][e1] * f, o[i][2 + e1] * f);
+          *reinterpret_cast<float2*>(dst + d) = make_float2(o[i][e1] * f, o[i][2 + e1] * f_odd);
         }
         if (!full && lg == 0) {
           float* ml = a.ws_ml + 2 * ((long long)(item + wid) * G + h);
@@ -776,7 +791,8 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
           v[jj] = (lg < NCOL)
-                      ? __uint_as_float((uint32_t)qst[(lg % G) * D + qk_d<MODE, D>(lt, s, jj)] << 16) * qmul
+                      ? __uint_as_float((uint32_t)qst[(lg % G) * D + qk_d<MODE, D>(lt, s, jj)] << 16) *
+                            ((MODE == INT4_PER_TOKEN_HEAD && jj >= 2) ? qmul * 0.0625f : qmul)
                       : 0.f;
         if constexpr (C::BF) {
           qf[s][0] = pack_bf16x2(v[0], v[1]);
