@@ -176,6 +176,24 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
                                 int max_context, float* out, int num_workers, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* kvq_decode_attention with a bf16 output: out is bf16 [batch][Hq][D]
+ * (16-byte aligned), each element the round-to-nearest-even bf16 of the fp32
+ * value kvq_decode_attention returns for the same arguments and num_workers.
+ * The pages leave the attention output's dtype open; this variant returns
+ * the model's native bf16 (the dtype [P3] "FP8 KV cache layer skipping vs
+ * per-head scales" keeps for unquantized layers) and halves the output
+ * traffic.  The arithmetic up to the final rounding is
+ * kvq_decode_attention's.  Arguments, errors and workspace as for
+ * kvq_decode_attention. */
+kvq_status kvq_decode_attention_bf16(const kvq_ctx* ctx, int layer, const void* q,
+                                     const void* k_cache, const void* v_cache,
+                                     const float* k_scale, const float* v_scale,
+                                     const float* k_cache_scale, const float* v_cache_scale,
+                                     const int* block_table, int max_blocks_per_seq,
+                                     const int* context_lens, int batch, int max_context,
+                                     void* out, int num_workers, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
 /* Decode attention that allocates nothing and needs no workspace from the
  * caller.  The pages have no counterpart to this call; it exists for callers
  * that cannot provide device scratch: code running where no device allocator

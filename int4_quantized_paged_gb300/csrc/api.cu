@@ -240,13 +240,18 @@ kvq_status kvq_decode_plan(const kvq_ctx* ctx, int layer, int batch, int max_con
   return KVQ_OK;
 }
 
-kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
-                                const void* k_cache, const void* v_cache, const float* k_scale,
-                                const float* v_scale, const float* k_cache_scale,
-                                const float* v_cache_scale, const int* block_table,
-                                int max_blocks_per_seq, const int* context_lens, int batch,
-                                int max_context, float* out, int num_workers, void* workspace,
-                                size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by the fp32- and bf16-output entry points: exactly one of out and
+// out_bf16 is non-null.
+kvq_status decode_impl(const kvq_ctx* ctx, int layer, const void* q, const void* k_cache,
+                       const void* v_cache, const float* k_scale, const float* v_scale,
+                       const float* k_cache_scale, const float* v_cache_scale,
+                       const int* block_table, int max_blocks_per_seq, const int* context_lens,
+                       int batch, int max_context, float* out, uint16_t* out_bf16,
+                       int num_workers, void* workspace, size_t workspace_bytes, void* stream) {
   kvq_status st = check_layer(ctx, layer);
   if (st != KVQ_OK) return st;
   if (batch < 0 || max_context < 0 || num_workers < 0 || max_blocks_per_seq < 0)
@@ -254,9 +259,10 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
   if (batch == 0) return KVQ_OK;
   const kvq_config& c = ctx->cfg;
   const int mode = ctx->mode[layer];
-  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
+  void* out_any = out ? static_cast<void*>(out) : static_cast<void*>(out_bf16);
+  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out_any)
     return KVQ_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out_any) ||
       !aligned4(block_table) || !aligned4(context_lens))
     return KVQ_ERR_ALIGNMENT;
   if ((mode == KVQ_FP8_PER_TENSOR || mode == KVQ_FP8_PER_HEAD) && (!k_scale || !v_scale))
@@ -286,6 +292,7 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
   a.block_table = block_table;
   a.context_lens = context_lens;
   a.out = out;
+  a.out_bf16 = out_bf16;
   float* ws = static_cast<float*>(workspace);
   const size_t n_part = ((size_t)batch * c.num_kv_heads + (size_t)workers) * G;
   a.ws_o = workers > 1 ? ws : nullptr;
@@ -305,6 +312,36 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
   a.qk_scale = ctx->softmax_scale * 1.4426950408889634f;
   return cuda_status(
       kvq::launch_decode(mode, c.head_dim, G, a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
+                                const void* k_cache, const void* v_cache, const float* k_scale,
+                                const float* v_scale, const float* k_cache_scale,
+                                const float* v_cache_scale, const int* block_table,
+                                int max_blocks_per_seq, const int* context_lens, int batch,
+                                int max_context, float* out, int num_workers, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  return decode_impl(ctx, layer, q, k_cache, v_cache, k_scale, v_scale, k_cache_scale,
+                     v_cache_scale, block_table, max_blocks_per_seq, context_lens, batch,
+                     max_context, out, nullptr, num_workers, workspace, workspace_bytes, stream);
+}
+
+kvq_status kvq_decode_attention_bf16(const kvq_ctx* ctx, int layer, const void* q,
+                                     const void* k_cache, const void* v_cache,
+                                     const float* k_scale, const float* v_scale,
+                                     const float* k_cache_scale, const float* v_cache_scale,
+                                     const int* block_table, int max_blocks_per_seq,
+                                     const int* context_lens, int batch, int max_context,
+                                     void* out, int num_workers, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  return decode_impl(ctx, layer, q, k_cache, v_cache, k_scale, v_scale, k_cache_scale,
+                     v_cache_scale, block_table, max_blocks_per_seq, context_lens, batch,
+                     max_context, nullptr, static_cast<uint16_t*>(out), num_workers, workspace,
+                     workspace_bytes, stream);
 }
 
 kvq_status kvq_e4m3_encode(const float* in, unsigned char* out, long long n, void* stream) {

@@ -542,8 +542,13 @@ __device__ void publish_items(const DecodeArgs& a, int lane) {
       if (a.item_tiles)
         for (int g = 0; g < a.Hkv; ++g) a.item_tiles[(long long)b * a.Hkv + g] = first + (long long)g * n;
       if (n == 0) {
-        float4* o = reinterpret_cast<float4*>(a.out + (long long)b * a.Hq * D);
-        for (int i = 0; i < a.Hq * D / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.out_bf16) {
+          uint4* o = reinterpret_cast<uint4*>(a.out_bf16 + (long long)b * a.Hq * D);
+          for (int i = 0; i < a.Hq * D / 8; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          float4* o = reinterpret_cast<float4*>(a.out + (long long)b * a.Hq * D);
+          for (int i = 0; i < a.Hq * D / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
     }
     base += __shfl_sync(0xffffffffu, incl, 31);
@@ -728,14 +733,23 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
         const int h = (G == 1) ? 0 : 2 * lt + e1;
         const float l = l_tot[e1];
         const float f = full ? (l > 0.f ? unscale / l : 0.f) : unscale;
-        float* dst = full ? a.out + (((long long)seg_b * a.Hq + seg_g * G + h) * D)
-                          : a.ws_o + (((long long)(item + wid) * G + h) * D);
+        const long long orow = ((long long)seg_b * a.Hq + seg_g * G + h) * D;
+        float* dst = full ? a.out + orow : a.ws_o + (((long long)(item + wid) * G + h) * D);
         // INT4: the odd-d rows were accumulated 16x (see pv_tile)
         const float f_odd = (MODE == INT4_PER_TOKEN_HEAD) ? f * 0.0625f : f;
+        if (full && a.out_bf16) {
 #pragma unroll
-        for (int i = 0; i < C::MTILES; ++i) {
-          const int d = lg * (D / 8) + 2 * i;
-          *reinterpret_cast<float2*>(dst + d) = make_float2(o[i][e1] * f, o[i][2 + e1] * f_odd);
+          for (int i = 0; i < C::MTILES; ++i) {
+            const int d = lg * (D / 8) + 2 * i;
+            *reinterpret_cast<uint32_t*>(a.out_bf16 + orow + d) =
+                pack_bf16x2(o[i][e1] * f, o[i][2 + e1] * f_odd);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < C::MTILES; ++i) {
+            const int d = lg * (D / 8) + 2 * i;
+            *reinterpret_cast<float2*>(dst + d) = make_float2(o[i][e1] * f, o[i][2 + e1] * f_odd);
+          }
         }
         if (!full && lg == 0) {
           float* ml = a.ws_ml + 2 * ((long long)(item + wid) * G + h);
@@ -1112,10 +1126,16 @@ __global__ void __launch_bounds__(32 * G) merge_kernel(const DecodeArgs a) {
     }
     M = Mn;
   }
-  float* out = a.out + ((long long)b * a.Hq + g * G + j) * D;
+  const long long orow = ((long long)b * a.Hq + g * G + j) * D;
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  if (a.out_bf16) {
 #pragma unroll
-  for (int k = 0; k < DL; ++k) out[lane + 32 * k] = acc[k] * inv;
+    for (int k = 0; k < DL; ++k)
+      a.out_bf16[orow + lane + 32 * k] = (uint16_t)(pack_bf16x2(acc[k] * inv, 0.f) & 0xFFFFu);
+  } else {
+#pragma unroll
+    for (int k = 0; k < DL; ++k) a.out[orow + lane + 32 * k] = acc[k] * inv;
+  }
 }
 
 // ------------------------------------------------------------------ host

@@ -42,7 +42,8 @@ struct DecodeArgs {
   const float* v_cs;
   const int* block_table;      // [B][max_blocks]
   const int* context_lens;     // [B]
-  float* out;                  // [B][Hq][D]
+  float* out;                  // [B][Hq][D] fp32, or
+  uint16_t* out_bf16;          // [B][Hq][D] bf16 (RN of the fp32 result) when non-null
   float* ws_o;                 // [B*Hkv + workers][G][D] unnormalised partial outputs
   float* ws_ml;                // [B*Hkv + workers][G][2] running max (log2 units) and sum
   long long* item_tiles;       // [B*Hkv + 1] first tile of each item in the tile list; T last

@@ -150,6 +150,22 @@ def test_decode_plan_and_workspace_rules():
                                   0, ok, 1, None, 0, None) == 0
 
 
+def test_bf16_output_decode_validates_like_fp32():
+    ctx = _ctx([3], Hq=64, Hkv=8, D=128)
+    _, ws5 = kvq.kvq_decode_plan(ctx, 0, 8, 131072, num_workers=5)
+    ok = 0x10000000
+    L = kvq._lib
+    f = L.kvq_decode_attention_bf16
+    assert f(ctx, 0, ok, ok, ok, None, None, ok, ok, ok, 8192, ok, 8, 131072, ok, 5, ok,
+             ws5 - 1, None) == 4                                 # workspace too small
+    assert f(ctx, 0, ok, ok, ok, None, None, ok, ok, ok, 8192, ok, 8, 131072, ok + 8, 1, None,
+             0, None) == 3                                        # output not 16-byte aligned
+    assert f(ctx, 0, ok, ok, ok, None, None, ok, ok, ok, 8192, ok, 8, 131072, None, 1, None, 0,
+             None) == 1                                           # no output
+    assert f(ctx, 0, ok, ok, ok, None, None, ok, ok, ok, 8192, ok, 0, 0, ok, 1, None, 0,
+             None) == 0                                           # empty batch
+
+
 def test_status_strings():
     for s in range(8):
         assert kvq.kvq_status_string(s)
