@@ -157,7 +157,11 @@ kvq_status kvq_decode_plan(const kvq_ctx* ctx, int layer, int batch, int max_con
  * q: bf16 [batch][Hq][D], 16-byte aligned.  Query head hq reads KV head
  *   hq / (Hq/Hkv).
  * block_table: int32 [batch][max_blocks_per_seq]; entries for positions that
- *   are not read may hold anything (e.g. -1).
+ *   are not read may hold anything (e.g. -1).  Only positions [lo, L) are
+ *   read, so a window layer may reuse its freed blocks as a ring: with
+ *   R = ceil(W / block_size) + 1 physical blocks per sequence, logical block j
+ *   may map to ring slot j mod R (the block a new position overwrites holds
+ *   only positions outside the window).
  * context_lens: int32 [batch]; L counts the current token, whose K/V were
  *   written first.  The query attends to positions [lo, L), lo = max(0, L-W)
  *   for a window W, else 0.  L = 0 gives a zero output row.

@@ -167,6 +167,25 @@ def paging(w: Workload, device, spare_blocks: int = 0) -> Paging:
     return Paging(bt.to(device), cl.to(device), total, maxb)
 
 
+def ring_paging(w: Workload, window: int, device) -> Paging:
+    """Paging of a window layer that reuses freed blocks: sequence b owns a
+    ring of R = ceil(W / bs) + 1 physical blocks and logical block j maps to
+    ring slot j mod R.  When position p is written, the block it overwrites
+    held positions below p + 1 - W, outside the window, so the retained
+    positions [L - W, L) always sit in distinct live blocks."""
+    bs = w.block_size
+    R = (window + bs - 1) // bs + 1
+    nb = [(L + bs - 1) // bs for L in w.context_lens]
+    maxb = max(max(nb), 1)
+    perm = torch.randperm(w.B * R, generator=_gen("cpu", w.seed, 3)).to(torch.int32)
+    bt = torch.full((w.B, maxb), -1, dtype=torch.int32)
+    for b, n in enumerate(nb):
+        ring = perm[b * R:(b + 1) * R]
+        bt[b, :n] = ring[torch.arange(n) % R]
+    cl = torch.tensor(w.context_lens, dtype=torch.int32)
+    return Paging(bt.to(device), cl.to(device), w.B * R, maxb)
+
+
 def slot_mapping(w: Workload, pg: Paging, positions: Sequence[range], device) -> torch.Tensor:
     """int64 slots for the given positions of each sequence, sequence-major."""
     bt = pg.block_table.cpu()

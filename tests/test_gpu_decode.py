@@ -14,6 +14,7 @@ import torch
 from int4_quantized_paged_gb300 import workloads as wl
 from oracle import oracle as orc
 from tests.gpu_harness import K, LayerRun, sample_pairs
+from tests.helpers import bits
 
 pytestmark = pytest.mark.gpu
 
@@ -130,3 +131,68 @@ def test_gemma_full_size_sampled(mode):
         r.write()
         out = r.decode()
         r.check_decode(out, pairs=sample_pairs(w, 16, seed=layer))
+
+
+@pytest.mark.parametrize("mode", [orc.FP8_PER_TOKEN_HEAD, orc.INT4_PER_TOKEN_HEAD, orc.BF16])
+def test_window_layer_ring_reuse_of_blocks(mode):
+    """A window layer paged as a ring of ceil(W/bs)+1 blocks per sequence,
+    filled with the retained positions and then advanced token by token
+    (each write overwrites a dead block), decodes exactly like the same layer
+    paged with one block per logical block, and matches the oracle."""
+    window = 40
+    base = wl.Workload("ring", Hq=32, Hkv=8, D=128, block_size=16,
+                       context_lens=(70, 300, 41, 1000), windows=(window,),
+                       head_mult_loguniform=(0.5, 32.0), outlier_p=0.01, outlier_factor=8.0,
+                       seed=91)
+    steps = 20
+    final = wl.Workload(**{**base.__dict__,
+                           "context_lens": tuple(L + steps for L in base.context_lens)})
+    kvq = K()
+    runs = {}
+    for kind in ("ring", "flat"):
+        r = LayerRun(final, mode)
+        if kind == "ring":
+            r.pg = wl.ring_paging(final, window, r.device)
+            r.ctx = kvq.kvq_create(1, final.Hq, final.Hkv, final.D, final.block_size,
+                                   r.pg.num_blocks, [mode], [window])
+            r.kc, r.vc, r.ks, r.vs = kvq.alloc_layer_cache(r.ctx, 0, r.device)
+        runs[kind] = r
+    # identical token streams for both layouts: the retained positions of the
+    # starting contexts, then `steps` single-token writes per sequence
+    for r in runs.values():
+        r.static_scales()
+    T0 = sum(min(L, window) for L in base.context_lens)
+    k0, v0 = wl.kv_tokens(final, T0, "cuda", stream_base=500)
+    pos0 = [torch.arange(max(0, L - window), L) for L in base.context_lens]
+    outs = {}
+    for kind, r in runs.items():
+        slots = wl.slot_mapping(final, r.pg, pos0, "cuda")
+        kvq.kvq_cache_write(r.ctx, 0, k0, v0, slots, r.kc, r.vc, r.ks, r.vs, r.k_scale, r.v_scale)
+    for s in range(steps):
+        ks_, vs_ = wl.kv_tokens(final, final.B, "cuda", stream_base=600 + s)
+        cl = torch.tensor([L + s + 1 for L in base.context_lens], dtype=torch.int32,
+                          device="cuda")
+        q = wl.queries(final, "cuda", layer=0)
+        for kind, r in runs.items():
+            slots = wl.slot_mapping(final, r.pg, [torch.tensor([L + s]) for L in base.context_lens],
+                                    "cuda")
+            kvq.kvq_cache_write(r.ctx, 0, ks_, vs_, slots, r.kc, r.vc, r.ks, r.vs,
+                                r.k_scale, r.v_scale)
+            out = r.decode(num_workers=0, context_lens=cl, q=q)
+            outs[kind] = out
+        assert torch.equal(outs["ring"].view(torch.int32), outs["flat"].view(torch.int32)), \
+            f"step {s}: ring-paged decode differs from the flat layout"
+    # the final state against the oracle, through the ring's own block table
+    r = runs["ring"]
+    kc, vc, ks, vs = orc.alloc_cache(mode, r.pg.num_blocks, final.Hkv, final.block_size, final.D)
+    slots0 = wl.slot_mapping(final, r.pg, pos0, "cuda")
+    orc.cache_write(mode, bits(k0), bits(v0), slots0.cpu().numpy(), kc, vc, ks, vs,
+                    k_scale=r.o_k_scale, v_scale=r.o_v_scale)
+    for s in range(steps):
+        ks_, vs_ = wl.kv_tokens(final, final.B, "cuda", stream_base=600 + s)
+        slots = wl.slot_mapping(final, r.pg, [torch.tensor([L + s]) for L in base.context_lens],
+                                "cuda")
+        orc.cache_write(mode, bits(ks_), bits(vs_), slots.cpu().numpy(), kc, vc, ks, vs,
+                        k_scale=r.o_k_scale, v_scale=r.o_v_scale)
+    r.host = (kc, vc, ks, vs)
+    r.check_decode(outs["ring"], where=f"ring mode {mode}")
