@@ -180,6 +180,28 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
                                 int max_context, float* out, int num_workers, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* kvq_decode_attention with an FP8 query.  Each query element x becomes the
+ * E4M3 code of RN32(x / q_scale) (round to nearest even, saturating to
+ * +-448, as kvq_cache_write encodes), and the scores use its value times
+ * q_scale: out = sum_p softmax(softmax_scale <q_hat, K_hat[p]>) V_hat[p] with
+ * q_hat = E4M3(q / q_scale) x q_scale.  This is the per-tensor FP8 path with
+ * one scale each for Q, K and V, and the per-attention-head path with one Q
+ * scale per query head ([P3] "FP8 KV cache layer skipping vs per-head
+ * scales", opening section).
+ * q_scale: device fp32, q_scale_count = 1 (one scale) or Hq (one per query
+ *   head), each finite and > 0.  Other arguments, errors and workspace as for
+ *   kvq_decode_attention; the output is fp32. */
+kvq_status kvq_decode_attention_fp8_query(const kvq_ctx* ctx, int layer, const void* q,
+                                          const float* q_scale, int q_scale_count,
+                                          const void* k_cache, const void* v_cache,
+                                          const float* k_scale, const float* v_scale,
+                                          const float* k_cache_scale,
+                                          const float* v_cache_scale, const int* block_table,
+                                          int max_blocks_per_seq, const int* context_lens,
+                                          int batch, int max_context, float* out,
+                                          int num_workers, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
 /* kvq_decode_attention with a bf16 output: out is bf16 [batch][Hq][D]
  * (16-byte aligned), each element the round-to-nearest-even bf16 of the fp32
  * value kvq_decode_attention returns for the same arguments and num_workers.

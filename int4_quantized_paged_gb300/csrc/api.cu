@@ -246,7 +246,8 @@ namespace {
 
 // Shared by the fp32- and bf16-output entry points: exactly one of out and
 // out_bf16 is non-null.
-kvq_status decode_impl(const kvq_ctx* ctx, int layer, const void* q, const void* k_cache,
+kvq_status decode_impl(const kvq_ctx* ctx, int layer, const void* q, const float* q_scale,
+                       int q_scale_count, const void* k_cache,
                        const void* v_cache, const float* k_scale, const float* v_scale,
                        const float* k_cache_scale, const float* v_cache_scale,
                        const int* block_table, int max_blocks_per_seq, const int* context_lens,
@@ -271,6 +272,10 @@ kvq_status decode_impl(const kvq_ctx* ctx, int layer, const void* q, const void*
     if (!k_cache_scale || !v_cache_scale) return KVQ_ERR_INVALID_ARG;
     if (!aligned4(k_cache_scale) || !aligned4(v_cache_scale)) return KVQ_ERR_ALIGNMENT;
   }
+  if (q_scale) {
+    if (q_scale_count != 1 && q_scale_count != c.num_q_heads) return KVQ_ERR_INVALID_ARG;
+    if (!aligned4(q_scale)) return KVQ_ERR_ALIGNMENT;
+  }
   int workers = num_workers;
   size_t need = 0;
   st = kvq_decode_plan(ctx, layer, batch, max_context, &workers, &need);
@@ -283,6 +288,8 @@ kvq_status decode_impl(const kvq_ctx* ctx, int layer, const void* q, const void*
   const int G = c.num_q_heads / c.num_kv_heads;
   kvq::DecodeArgs a;
   a.q = static_cast<const uint16_t*>(q);
+  a.q_scale = q_scale;
+  a.q_scale_count = q_scale ? q_scale_count : 0;
   a.k_cache = static_cast<const uint8_t*>(k_cache);
   a.v_cache = static_cast<const uint8_t*>(v_cache);
   a.k_scale = k_scale;
@@ -325,9 +332,27 @@ kvq_status kvq_decode_attention(const kvq_ctx* ctx, int layer, const void* q,
                                 int max_blocks_per_seq, const int* context_lens, int batch,
                                 int max_context, float* out, int num_workers, void* workspace,
                                 size_t workspace_bytes, void* stream) {
-  return decode_impl(ctx, layer, q, k_cache, v_cache, k_scale, v_scale, k_cache_scale,
-                     v_cache_scale, block_table, max_blocks_per_seq, context_lens, batch,
-                     max_context, out, nullptr, num_workers, workspace, workspace_bytes, stream);
+  return decode_impl(ctx, layer, q, nullptr, 0, k_cache, v_cache, k_scale, v_scale,
+                     k_cache_scale, v_cache_scale, block_table, max_blocks_per_seq, context_lens,
+                     batch, max_context, out, nullptr, num_workers, workspace, workspace_bytes,
+                     stream);
+}
+
+kvq_status kvq_decode_attention_fp8_query(const kvq_ctx* ctx, int layer, const void* q,
+                                          const float* q_scale, int q_scale_count,
+                                          const void* k_cache, const void* v_cache,
+                                          const float* k_scale, const float* v_scale,
+                                          const float* k_cache_scale,
+                                          const float* v_cache_scale, const int* block_table,
+                                          int max_blocks_per_seq, const int* context_lens,
+                                          int batch, int max_context, float* out,
+                                          int num_workers, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  if (!q_scale) return KVQ_ERR_INVALID_ARG;
+  return decode_impl(ctx, layer, q, q_scale, q_scale_count, k_cache, v_cache, k_scale, v_scale,
+                     k_cache_scale, v_cache_scale, block_table, max_blocks_per_seq, context_lens,
+                     batch, max_context, out, nullptr, num_workers, workspace, workspace_bytes,
+                     stream);
 }
 
 kvq_status kvq_decode_attention_bf16(const kvq_ctx* ctx, int layer, const void* q,
@@ -338,10 +363,10 @@ kvq_status kvq_decode_attention_bf16(const kvq_ctx* ctx, int layer, const void* 
                                      const int* context_lens, int batch, int max_context,
                                      void* out, int num_workers, void* workspace,
                                      size_t workspace_bytes, void* stream) {
-  return decode_impl(ctx, layer, q, k_cache, v_cache, k_scale, v_scale, k_cache_scale,
-                     v_cache_scale, block_table, max_blocks_per_seq, context_lens, batch,
-                     max_context, nullptr, static_cast<uint16_t*>(out), num_workers, workspace,
-                     workspace_bytes, stream);
+  return decode_impl(ctx, layer, q, nullptr, 0, k_cache, v_cache, k_scale, v_scale,
+                     k_cache_scale, v_cache_scale, block_table, max_blocks_per_seq, context_lens,
+                     batch, max_context, nullptr, static_cast<uint16_t*>(out), num_workers,
+                     workspace, workspace_bytes, stream);
 }
 
 kvq_status kvq_e4m3_encode(const float* in, unsigned char* out, long long n, void* stream) {

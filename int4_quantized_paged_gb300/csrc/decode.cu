@@ -124,6 +124,16 @@ __device__ __forceinline__ float f16_lo(uint32_t h2) {
 }
 __device__ __forceinline__ float bf16_lo(uint32_t h2) { return __uint_as_float(h2 << 16); }
 
+// y rounded to E4M3 (nearest even, saturating to +-448), as a float: the
+// value of the code the cache write would store for y.
+__device__ __forceinline__ float e4m3_round(float y) {
+  unsigned short c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(0.f), "f"(y));
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  return f16_lo(h2);
+}
+
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t r;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
@@ -677,6 +687,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
   float acc[NT][C::MTILES][4];
   int vexp = -1000;               // running max exponent of the V scales (dynamic)
   float fv = 0.f;                 // 2^(KP - vexp)
+  float qc[2] = {1.f, 1.f};       // per-column query scale (FP8 query, per-head scales)
   int seg_b = -1, seg_g = -1, seg_k0 = 0, seg_klast = 0, seg_n = 0;
 
   // Writes the segment's result: final output if it covered the whole item,
@@ -793,21 +804,34 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       __syncwarp();
       int qexp = 0;                   // q is scaled by 2^(14 - qexp) for f16
-      if (!C::BF && amax > 0.f)
+      if (!C::BF && amax > 0.f && !a.q_scale)
         qexp = max(((int)(__float_as_uint(amax) >> 23) & 0xFF) - 127, -100);
-      const float qmul = C::BF ? 1.f : pow2i(14 - qexp);
+      const float qmul = (C::BF || a.q_scale) ? 1.f : pow2i(14 - qexp);
       float ks = ks_static;
       if constexpr (MODE == FP8_PER_HEAD) ks = a.k_scale[seg_g];
-      s_fac = a.qk_scale * ks * (C::BF ? 1.f : pow2i(qexp - 14));
+      s_fac = a.qk_scale * ks * ((C::BF || a.q_scale) ? 1.f : pow2i(qexp - 14));
+      // FP8 query: every element becomes the E4M3 value of RN32(q / q_scale)
+      // (exact in f16 and bf16) and q_scale multiplies the score: a single
+      // scale folds into s_fac, per-head scales into the column factors qc
+      float qs_col = 1.f;             // scale of this lane's staged column (lg)
+      if (a.q_scale) {
+        const bool per_head = a.q_scale_count > 1;
+        if (!per_head) s_fac *= a.q_scale[0];
+        qs_col = a.q_scale[per_head ? seg_g * G + (lg % G) : 0];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) qc[e] = per_head ? a.q_scale[seg_g * G + ((2 * lt + e) % G)] : 1.f;
+      }
 #pragma unroll
       for (int s = 0; s < C::KSTEPS; ++s) {
         float v[4];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          v[jj] = (lg < NCOL)
-                      ? __uint_as_float((uint32_t)qst[(lg % G) * D + qk_d<MODE, D>(lt, s, jj)] << 16) *
-                            ((MODE == INT4_PER_TOKEN_HEAD && jj >= 2) ? qmul * 0.0625f : qmul)
-                      : 0.f;
+        for (int jj = 0; jj < 4; ++jj) {
+          float x = (lg < NCOL)
+                        ? __uint_as_float((uint32_t)qst[(lg % G) * D + qk_d<MODE, D>(lt, s, jj)] << 16)
+                        : 0.f;
+          if (a.q_scale) x = e4m3_round(__fdiv_rn(x, qs_col));
+          v[jj] = x * ((MODE == INT4_PER_TOKEN_HEAD && jj >= 2) ? qmul * 0.0625f : qmul);
+        }
         if constexpr (C::BF) {
           qf[s][0] = pack_bf16x2(v[0], v[1]);
           qf[s][1] = pack_bf16x2(v[2], v[3]);
@@ -883,7 +907,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
       for (int e = 0; e < 4; ++e) {
         const int pos = pos0 + u * TILE + lg + ((e & 2) ? 8 : 0);
         const bool v = ok[u] && (whole || (pos >= lo && pos < L)) && (2 * lt + (e & 1)) < NCOL;
-        s_raw[u][e] = v ? sacc[u][e] * (e < 2 ? kf0 : kf1) : -INFINITY;
+        s_raw[u][e] = v ? sacc[u][e] * (e < 2 ? kf0 : kf1) * qc[e & 1] : -INFINITY;
       }
     }
 

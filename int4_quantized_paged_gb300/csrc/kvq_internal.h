@@ -34,6 +34,8 @@ struct WriteArgs {
 
 struct DecodeArgs {
   const uint16_t* q;           // bf16 [B][Hq][D]
+  const float* q_scale;        // FP8 query: [1] or [Hq] scales (nullptr: bf16 query)
+  int q_scale_count;
   const uint8_t* k_cache;
   const uint8_t* v_cache;
   const float* k_scale;        // static modes: [1] or [Hkv]

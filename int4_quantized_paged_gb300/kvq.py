@@ -56,6 +56,8 @@ _SIGS = {
     "kvq_decode_plan": (i32, [P, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(sz)]),
     "kvq_decode_attention": (i32, [P, i32, P, P, P, P, P, P, P, P, i32, P, i32, i32, P, i32, P,
                                    sz, P]),
+    "kvq_decode_attention_fp8_query": (i32, [P, i32, P, P, i32, P, P, P, P, P, P, P, i32, P, i32,
+                                             i32, P, i32, P, sz, P]),
     "kvq_decode_attention_bf16": (i32, [P, i32, P, P, P, P, P, P, P, P, i32, P, i32, i32, P, i32,
                                         P, sz, P]),
     "kvq_decode_attention_fixed_scratch": (i32, [P, i32, P, P, P, P, P, P, P, P, i32, P, i32,
@@ -204,6 +206,26 @@ def kvq_decode_attention(ctx: Context, layer: int, q, k_cache, v_cache, block_ta
                                      _ptr(context_lens), B, max_context, _ptr(out), num_workers,
                                      _ptr(workspace), workspace_bytes, _stream(stream)),
            "kvq_decode_attention")
+
+
+def kvq_decode_attention_fp8_query(ctx: Context, layer: int, q, q_scale, k_cache, v_cache,
+                                   block_table, context_lens, out, *, max_context: int,
+                                   k_scale=None, v_scale=None, k_cache_scale=None,
+                                   v_cache_scale=None, num_workers: int = 0, workspace=None,
+                                   workspace_bytes: Optional[int] = None,
+                                   batch: Optional[int] = None,
+                                   max_blocks_per_seq: Optional[int] = None, stream=None):
+    """kvq_decode_attention with the query quantized to E4M3 by q_scale (a
+    device fp32 tensor of 1 or Hq scales)."""
+    B = q.shape[0] if batch is None else batch
+    mb = block_table.shape[1] if max_blocks_per_seq is None else max_blocks_per_seq
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.kvq_decode_attention_fp8_query(
+        ctx, layer, _ptr(q), _ptr(q_scale), q_scale.numel(), _ptr(k_cache), _ptr(v_cache),
+        _ptr(k_scale), _ptr(v_scale), _ptr(k_cache_scale), _ptr(v_cache_scale),
+        _ptr(block_table), mb, _ptr(context_lens), B, max_context, _ptr(out), num_workers,
+        _ptr(workspace), workspace_bytes, _stream(stream)), "kvq_decode_attention_fp8_query")
 
 
 def kvq_decode_attention_bf16(ctx: Context, layer: int, q, k_cache, v_cache, block_table,

@@ -192,6 +192,47 @@ def decode(mode, q, k_cache, v_cache, block_table, context_lens, *, k_scale=None
     return out.reshape(B, Hq, D) if pairs is None else out
 
 
+def quantize_query(q, q_scale):
+    """FP8 query of the Q-scale path (the pages' per-tensor FP8 with one Q
+    scale, or one Q scale per query head: [P3] "FP8 KV cache layer skipping vs
+    per-head scales", opening section).  Each element x of q (bf16 bits
+    [B, Hq, D]) becomes the E4M3 code of y = RN32(x / s) (IEEE fp32 division,
+    then round to nearest even, saturating), s = q_scale[0] or q_scale[hq].
+    Returns the bf16 bits of the codes' values (E4M3 values are exact in
+    bf16) and the per-head scales [Hq] as float64."""
+    q = _u16(q)
+    B, Hq, D = q.shape
+    qs = np.asarray(q_scale, dtype=np.float32).reshape(-1)
+    s = np.broadcast_to(qs, (Hq,)) if qs.size == 1 else qs
+    x = (q.astype(np.uint32) << 16).view(np.float32)
+    y = np.ascontiguousarray(x / s[None, :, None], dtype=np.float32)   # fp32 RN division
+    codes = np.empty(y.shape, dtype=np.uint8)
+    lib().orc_e4m3_encode_array(y.ctypes.data, codes.ctypes.data, y.size)
+    vals = e4m3_decode_table()[codes].astype(np.float32)
+    return (vals.view(np.uint32) >> 16).astype(np.uint16), s.astype(np.float64)
+
+
+def decode_fp8_query(mode, q, q_scale, k_cache, v_cache, block_table, context_lens, *,
+                     softmax_scale=0.0, pairs=None, **kw):
+    """float64 decode with the FP8 query q_hat = E4M3(q / s) x s: the scores
+    are softmax_scale x s x <E4M3 value, K_hat>, so each query head is decoded
+    with its own factor.  Same returns as decode."""
+    codes, s = quantize_query(q, q_scale)
+    B, Hq, D = codes.shape
+    if softmax_scale == 0.0:
+        softmax_scale = 1.0 / np.sqrt(D)
+    if pairs is None:
+        pairs = [(b, h) for b in range(B) for h in range(Hq)]
+    pairs = [tuple(p) for p in pairs]
+    out = np.zeros((len(pairs), D), dtype=np.float64)
+    for h in sorted(set(p[1] for p in pairs)):
+        idx = [i for i, p in enumerate(pairs) if p[1] == h]
+        out[idx] = decode(mode, codes, k_cache, v_cache, block_table, context_lens,
+                          softmax_scale=float(softmax_scale * s[h]),
+                          pairs=[pairs[i] for i in idx], **kw)
+    return out
+
+
 def dequantize(mode, k_cache, k_cache_scale=None, k_scale=None):
     """Dequantized cache values [num_blocks, Hkv, bs, D] in float64 (for tests)."""
     table = e4m3_decode_table()
