@@ -220,6 +220,34 @@ kvq_status kvq_decode_attention_bf16(const kvq_ctx* ctx, int layer, const void* 
                                      void* out, int num_workers, void* workspace,
                                      size_t workspace_bytes, void* stream);
 
+/* Prefill (chunked multi-query) attention over the quantized paged cache:
+ * the new tokens of each sequence attend causally to the cache, as at the
+ * prefill stage whose time to first token the pages record ([P3] "FP8 KV
+ * cache layer skipping vs per-head scales", section "Run a four-way
+ * ablation").
+ *
+ * Sequence b has n_b = query_start[b+1] - query_start[b] new tokens at
+ * positions [L_b - n_b, L_b), L_b = context_lens[b] >= n_b; their K/V were
+ * written first (kvq_cache_write).  Query row query_start[b] + i of q (bf16
+ * [T][Hq][D], T = query_start[batch], 16-byte aligned) sits at position
+ * p = L_b - n_b + i and attends to positions [lo(p), p], lo(p) =
+ * max(0, p + 1 - W) for a window W, else 0; out (fp32 [T][Hq][D]) is the
+ * softmax(softmax_scale <q, K_hat>) weighted sum of V_hat over them, exactly
+ * what kvq_decode_attention returns for that query with context p + 1.
+ * query_start: int32 [batch + 1], query_start[0] = 0, non-decreasing.
+ * max_query_len: an upper bound of every n_b (sizes the grid; rows past n_b
+ *   do no work).
+ * Scale pointers and block table as for kvq_decode_attention.  No workspace;
+ * n_b > L_b sets the BAD_INDEX bit of the device error word and skips that
+ * sequence. */
+kvq_status kvq_prefill_attention(const kvq_ctx* ctx, int layer, const void* q,
+                                 const void* k_cache, const void* v_cache, const float* k_scale,
+                                 const float* v_scale, const float* k_cache_scale,
+                                 const float* v_cache_scale, const int* block_table,
+                                 int max_blocks_per_seq, const int* query_start,
+                                 const int* context_lens, int batch, int max_query_len,
+                                 float* out, void* stream);
+
 /* Decode attention that allocates nothing and needs no workspace from the
  * caller.  The pages have no counterpart to this call; it exists for callers
  * that cannot provide device scratch: code running where no device allocator

@@ -369,6 +369,62 @@ kvq_status kvq_decode_attention_bf16(const kvq_ctx* ctx, int layer, const void* 
                      workspace, workspace_bytes, stream);
 }
 
+kvq_status kvq_prefill_attention(const kvq_ctx* ctx, int layer, const void* q,
+                                 const void* k_cache, const void* v_cache, const float* k_scale,
+                                 const float* v_scale, const float* k_cache_scale,
+                                 const float* v_cache_scale, const int* block_table,
+                                 int max_blocks_per_seq, const int* query_start,
+                                 const int* context_lens, int batch, int max_query_len,
+                                 float* out, void* stream) {
+  kvq_status st = check_layer(ctx, layer);
+  if (st != KVQ_OK) return st;
+  if (batch < 0 || max_query_len < 0 || max_blocks_per_seq < 0) return KVQ_ERR_INVALID_ARG;
+  if (batch == 0 || max_query_len == 0) return KVQ_OK;
+  const kvq_config& c = ctx->cfg;
+  const int mode = ctx->mode[layer];
+  if (!q || !k_cache || !v_cache || !block_table || !query_start || !context_lens || !out)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned4(block_table) || !aligned4(query_start) || !aligned4(context_lens))
+    return KVQ_ERR_ALIGNMENT;
+  if ((mode == KVQ_FP8_PER_TENSOR || mode == KVQ_FP8_PER_HEAD) && (!k_scale || !v_scale))
+    return KVQ_ERR_INVALID_ARG;
+  if (is_dynamic(mode)) {
+    if (!k_cache_scale || !v_cache_scale) return KVQ_ERR_INVALID_ARG;
+    if (!aligned4(k_cache_scale) || !aligned4(v_cache_scale)) return KVQ_ERR_ALIGNMENT;
+  }
+  const int G = c.num_q_heads / c.num_kv_heads;
+  const long long qtiles = ((long long)max_query_len * G + kvq::prefill_rows_per_cta() - 1) /
+                           kvq::prefill_rows_per_cta();
+  if (qtiles * batch * c.num_kv_heads >= (1LL << 31)) return KVQ_ERR_INVALID_ARG;
+  unsigned* err = kvq::error_word();
+  if (!err) return KVQ_ERR_CUDA;
+  kvq::DecodeArgs a = {};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k_cache = static_cast<const uint8_t*>(k_cache);
+  a.v_cache = static_cast<const uint8_t*>(v_cache);
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.k_cs = k_cache_scale;
+  a.v_cs = v_cache_scale;
+  a.block_table = block_table;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.err = err;
+  a.B = batch;
+  a.Hq = c.num_q_heads;
+  a.Hkv = c.num_kv_heads;
+  a.bs = c.block_size;
+  a.bs_shift = __builtin_ctz((unsigned)c.block_size);
+  a.max_blocks = max_blocks_per_seq;
+  a.window = ctx->window[layer];
+  a.workers = 1;
+  a.num_blocks = c.num_blocks;
+  a.qk_scale = ctx->softmax_scale * 1.4426950408889634f;
+  return cuda_status(kvq::launch_prefill(mode, c.head_dim, G, a, query_start, max_query_len,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_e4m3_encode(const float* in, unsigned char* out, long long n, void* stream) {
   if (n < 0 || (n > 0 && (!in || !out))) return KVQ_ERR_INVALID_ARG;
   return cuda_status(kvq::launch_e4m3_encode(in, out, n, static_cast<cudaStream_t>(stream)));

@@ -49,6 +49,7 @@
 
 #include "async_copy.cuh"
 #include "kvq_internal.h"
+#include "tile_math.cuh"
 
 namespace kvq {
 namespace {
@@ -63,112 +64,6 @@ constexpr int WARPS = 4;         // worker warps per CTA (independent)
 constexpr int PAIR = KVQ_TILES_PER_ITER;   // 16-position tiles per loop iteration
 constexpr int TILE = 16;         // positions per tile
 constexpr int KP = 13;           // P' = p v_scale 2^(KP - vexp) < 2^14 (dynamic scales)
-
-// ------------------------------------------------------------------ PTX
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ void tma_tile_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Four E4M3 codes (one word) -> two f16x2: bytes 0,1 -> lo; bytes 2,3 -> hi.
-// The conversion is exact.
-__device__ __forceinline__ void e4m3x4_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.rn.f16x2.e4m3x2 %0, a; cvt.rn.f16x2.e4m3x2 %1, b; }"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-}
-
-// The two's-complement nibbles at bits 4P..4P+3 and 16+4P..19+4P of x (P = 0
-// or 1) -> f16x2 of 16^P times their signed values, exactly.  Flipping bit 3
-// of a nibble makes it offset binary m = n + 8; placed in the mantissa under
-// the exponent of 1024 it reads 1024 + 16^P m, and subtracting 1024 + 8 16^P
-// leaves 16^P n.  The flip, the mask and the exponent bits are one
-// three-input logic operation.
-template <int P>
-__device__ __forceinline__ uint32_t nib2_f16x2(uint32_t x) {
-  constexpr uint32_t M = 0x000F000Fu << (4 * P);
-  constexpr uint32_t C = (0x00080008u << (4 * P)) | 0x64006400u;
-  constexpr uint32_t S = P == 0 ? 0x64086408u : 0x64806480u;   // f16 1032 / 1152
-  const uint32_t h = (x & M) ^ C;
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(S));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ float f16_lo(uint32_t h2) {
-  float f;
-  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %1; cvt.f32.f16 %0, a; }" : "=f"(f) : "r"(h2));
-  return f;
-}
-__device__ __forceinline__ float bf16_lo(uint32_t h2) { return __uint_as_float(h2 << 16); }
-
-// y rounded to E4M3 (nearest even, saturating to +-448), as a float: the
-// value of the code the cache write would store for y.
-__device__ __forceinline__ float e4m3_round(float y) {
-  unsigned short c;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(0.f), "f"(y));
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
-  return f16_lo(h2);
-}
-
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-  uint32_t r;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
-  return r;
-}
-
-template <bool BF>
-__device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32_t b0,
-                                         uint32_t b1) {
-  if constexpr (BF) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-}
-
-// ------------------------------------------------------------------ layout
-template <int MODE>
-constexpr int row_bytes(int D) {
-  return MODE == BF16 ? 2 * D : (MODE == INT4_PER_TOKEN_HEAD ? D / 2 : D);
-}
-
-// Shared-memory byte offset of logical byte `o` of a tile written by a TMA
-// copy with 128-byte rows and 128B swizzle (buffer 1024-byte aligned).
-__device__ __forceinline__ uint32_t swz(uint32_t o) {
-  return o ^ (((o >> 7) & 7u) << 4);
-}
 
 template <int N>
 __device__ __forceinline__ void lds(uint32_t (&r)[N], const uint8_t* base, uint32_t o) {
@@ -235,16 +130,6 @@ __device__ __forceinline__ void load_seg(uint32_t* w, const uint8_t* tile, uint3
     lds<1>(r, tile, off);
     w[0] = ok ? r[0] : 0u;
   }
-}
-
-// 2^e for e in [-126, 127] (exact, from the exponent bits); 0 below.
-__device__ __forceinline__ float pow2i(int e) {
-  return e < -126 ? 0.f : __uint_as_float((uint32_t)(e + 127) << 23);
-}
-
-// Unbiased exponent of a positive normal float.
-__device__ __forceinline__ int f32_exp(float x) {
-  return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
 }
 
 // QK of one 16-position sub-tile: sacc (rows lg, lg+8; columns 2lt, 2lt+1)
@@ -413,7 +298,6 @@ struct Layout {
 #endif
   static constexpr int ring = NS * C::STAGE;
   static constexpr int scales = NS * C::SCALES;
-  static constexpr int bars = NS * 8;
   static constexpr int aux = aux_of(NS);
   static constexpr int total = WARPS * (ring + aux) + 1024;   // + alignment slack
 };
@@ -1163,40 +1047,6 @@ __global__ void __launch_bounds__(32 * G) merge_kernel(const DecodeArgs a) {
 }
 
 // ------------------------------------------------------------------ host
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn encode_fn() {
-  static EncodeFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(p);
-  }
-  return fn;
-}
-
-// The layer's code buffer as a 2-D uint8 tensor of 128-byte rows; one box is
-// a 16-position tile of one (block, KV head) page.
-bool make_map(CUtensorMap* m, const void* base, long long total_bytes, int tile_bytes) {
-  EncodeFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {128, (cuuint64_t)(total_bytes / 128)};
-  cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {128, (cuuint32_t)(tile_bytes / 128)};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Sets the kernel's dynamic shared-memory limit once per device; returns its
 // resident CTAs per SM (0 on failure).
 template <int MODE, int D, int G>
@@ -1227,7 +1077,7 @@ cudaError_t launch3(const DecodeArgs& a, cudaStream_t st) {
   const long long total = a.num_blocks * a.Hkv * a.bs * (long long)C::RB;
   CUtensorMap km, vm;
   if (total > 0) {
-    if (!make_map(&km, a.k_cache, total, C::TB) || !make_map(&vm, a.v_cache, total, C::TB))
+    if (!make_tile_map(&km, a.k_cache, total, C::TB) || !make_tile_map(&vm, a.v_cache, total, C::TB))
       return cudaErrorInvalidValue;
   }
   int smem = 0;
@@ -1307,6 +1157,40 @@ cudaError_t launch1(int D, int G, const DecodeArgs& a, cudaStream_t st) {
 }
 
 }  // namespace
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+// The layer's code buffer as a 2-D uint8 tensor of 128-byte rows; one box is
+// a 16-position tile of one (block, KV head) page.
+bool make_tile_map(CUtensorMap* m, const void* base, long long total_bytes, int tile_bytes) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)(total_bytes / 128)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, (cuuint32_t)(tile_bytes / 128)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int decode_ctas_per_sm(int mode, int D, int G) {
   switch (mode) {

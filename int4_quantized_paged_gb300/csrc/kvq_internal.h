@@ -2,6 +2,7 @@
 // translation units.  Not installed; not part of the ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -63,9 +64,18 @@ cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, long long n, cudaS
 // Returns cudaErrorInvalidValue for an unsupported (mode, D, G) combination.
 cudaError_t launch_decode(int mode, int D, int G, const DecodeArgs& a, cudaStream_t st);
 bool decode_supported(int mode, int D, int G);
+// Prefill: one CTA per (query tile, sequence, KV head); DecodeArgs supplies the
+// caches, scales, block table, context lengths, q and out (no workspace).
+cudaError_t launch_prefill(int mode, int D, int G, const DecodeArgs& a, const int* query_start,
+                           int max_query_len, cudaStream_t st);
+int prefill_rows_per_cta();
 // Resident decode CTAs per SM on the current device (0 if unknown: no device).
 int decode_ctas_per_sm(int mode, int D, int G);
 int decode_warps_per_cta();
+
+// 2-D TMA map of a layer's code buffer viewed as [total_bytes / 128] rows of
+// 128 bytes, box of tile_bytes / 128 rows, 128B swizzle (false on failure).
+bool make_tile_map(CUtensorMap* m, const void* base, long long total_bytes, int tile_bytes);
 
 // Device error word of the current device.
 unsigned* error_word();

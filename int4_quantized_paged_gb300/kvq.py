@@ -56,6 +56,7 @@ _SIGS = {
     "kvq_decode_plan": (i32, [P, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(sz)]),
     "kvq_decode_attention": (i32, [P, i32, P, P, P, P, P, P, P, P, i32, P, i32, i32, P, i32, P,
                                    sz, P]),
+    "kvq_prefill_attention": (i32, [P, i32, P, P, P, P, P, P, P, P, i32, P, P, i32, i32, P, P]),
     "kvq_decode_attention_fp8_query": (i32, [P, i32, P, P, i32, P, P, P, P, P, P, P, i32, P, i32,
                                              i32, P, i32, P, sz, P]),
     "kvq_decode_attention_bf16": (i32, [P, i32, P, P, P, P, P, P, P, P, i32, P, i32, i32, P, i32,
@@ -206,6 +207,22 @@ def kvq_decode_attention(ctx: Context, layer: int, q, k_cache, v_cache, block_ta
                                      _ptr(context_lens), B, max_context, _ptr(out), num_workers,
                                      _ptr(workspace), workspace_bytes, _stream(stream)),
            "kvq_decode_attention")
+
+
+def kvq_prefill_attention(ctx: Context, layer: int, q, k_cache, v_cache, block_table,
+                          query_start, context_lens, out, *, max_query_len: int, k_scale=None,
+                          v_scale=None, k_cache_scale=None, v_cache_scale=None,
+                          batch: Optional[int] = None, max_blocks_per_seq: Optional[int] = None,
+                          stream=None):
+    """Causal attention of each sequence's new tokens (rows of q between
+    query_start[b] and query_start[b+1]) over the cache; see include/kvq.h."""
+    B = context_lens.shape[0] if batch is None else batch
+    mb = block_table.shape[1] if max_blocks_per_seq is None else max_blocks_per_seq
+    _check(_lib.kvq_prefill_attention(ctx, layer, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(k_scale), _ptr(v_scale), _ptr(k_cache_scale),
+                                      _ptr(v_cache_scale), _ptr(block_table), mb,
+                                      _ptr(query_start), _ptr(context_lens), B, max_query_len,
+                                      _ptr(out), _stream(stream)), "kvq_prefill_attention")
 
 
 def kvq_decode_attention_fp8_query(ctx: Context, layer: int, q, q_scale, k_cache, v_cache,

@@ -192,6 +192,29 @@ def decode(mode, q, k_cache, v_cache, block_table, context_lens, *, k_scale=None
     return out.reshape(B, Hq, D) if pairs is None else out
 
 
+def prefill(mode, q, k_cache, v_cache, block_table, query_start, context_lens, *, pairs=None,
+            **kw):
+    """float64 prefill attention: row query_start[b] + i of q (bf16 bits
+    [T, Hq, D]) is the query at position p = L_b - n_b + i of sequence b, and
+    its output is the decode of that query with context p + 1 (positions
+    [lo(p), p], causal; the window and scales as in decode).  Returns
+    [T, Hq, D], or [len(pairs), D] for pairs (token, hq)."""
+    q = _u16(q)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    qs = np.asarray(query_start, dtype=np.int64)
+    cl = np.asarray(context_lens, dtype=np.int64)
+    T = int(qs[-1])
+    seq = np.zeros(T, dtype=np.int64)
+    ctx = np.zeros(T, dtype=np.int32)
+    for b in range(len(cl)):
+        n = int(qs[b + 1] - qs[b])
+        if n <= 0:
+            continue
+        seq[qs[b]:qs[b + 1]] = b
+        ctx[qs[b]:qs[b + 1]] = int(cl[b]) - n + 1 + np.arange(n)
+    return decode(mode, q, k_cache, v_cache, bt[seq], ctx, pairs=pairs, **kw)
+
+
 def quantize_query(q, q_scale):
     """FP8 query of the Q-scale path (the pages' per-tensor FP8 with one Q
     scale, or one Q scale per query head: [P3] "FP8 KV cache layer skipping vs
