@@ -689,6 +689,105 @@ def run_latency_sweep(args):
     return res
 
 
+PREFILL = {
+    "llama8b": ("llama8b-like prefill chunk: 4 sequences x 1024 new tokens after 3072 cached, "
+                "Hq=32 Hkv=8 D=128", 4, 3072, 1024),
+    "gemma_d256": ("Gemma-like prefill chunk: 8192 new tokens at positions [8192, 16384) of one "
+                   "sequence, Hq=16 Hkv=8 D=256, full-attention layer", 1, 8192, 8192),
+}
+
+
+def peak_tensor():
+    """Dense bf16 tensor peak (TFLOP/s) and its source."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        for k in ("bf16_tflops", "bf16_dense_tflops"):
+            if k in d:
+                return float(d[k]), "measured"
+    except (OSError, ValueError):
+        pass
+    return 1900.0, "fallback"
+
+
+def run_prefill(args):
+    """Prefill attention (kvq_prefill_attention) on one chunk shape: time and
+    TFLOP/s of the causal QK and PV products (4 D flop per query-key pair)."""
+    import torch
+    from int4_quantized_paged_gb300 import kvq
+    from int4_quantized_paged_gb300 import workloads as wl
+
+    if args.workload not in PREFILL:
+        raise SystemExit(f"--prefill: no chunk shape for workload {args.workload}; "
+                         f"choose one of {sorted(PREFILL)}")
+    desc, B, prefix, chunk = PREFILL[args.workload]
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    base = wl.CONFIGS[args.workload]
+    L = prefix + chunk
+    w = wl.Workload(**{**base.__dict__, "context_lens": tuple([L] * B), "windows": (0,)})
+    mode = kvq.MODE_NAMES[args.mode]
+    pg = wl.paging(w, dev)
+    ctx = kvq.kvq_create(1, w.Hq, w.Hkv, w.D, w.block_size, pg.num_blocks, [mode], [0])
+    kc, vc, ks, vs = kvq.alloc_layer_cache(ctx, 0, dev)
+    k_scale = v_scale = None
+    if mode in (kvq.FP8_PER_TENSOR, kvq.FP8_PER_HEAD):
+        k_scale = torch.ones(w.Hkv if mode == kvq.FP8_PER_HEAD else 1, device=dev)
+        v_scale = k_scale.clone()
+    for b in range(B):
+        pos = [torch.tensor([], dtype=torch.int64)] * b + [torch.arange(L)]
+        k, v = wl.kv_tokens(w, L, dev, stream_base=40 + b)
+        kvq.kvq_cache_write(ctx, 0, k, v, wl.slot_mapping(w, pg, pos, dev), kc, vc, ks, vs,
+                            k_scale, v_scale)
+    T = B * chunk
+    g = torch.Generator(device=dev).manual_seed(base.seed + 77)
+    q = torch.randn(T, w.Hq, w.D, generator=g, device=dev).to(torch.bfloat16)
+    qs = torch.arange(0, T + 1, chunk, dtype=torch.int32, device=dev)
+    out = torch.empty(T, w.Hq, w.D, dtype=torch.float32, device=dev)
+
+    def step():
+        kvq.kvq_prefill_attention(ctx, 0, q, kc, vc, pg.block_table, qs, pg.context_lens, out,
+                                  max_query_len=chunk, k_scale=k_scale, v_scale=v_scale,
+                                  k_cache_scale=ks, v_cache_scale=vs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if kvq.kvq_get_device_error() != 0:
+        raise RuntimeError("device error word set during prefill warm-up")
+    n = args.steps if args.steps > 0 else 10
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(0)
+    sampler.start()
+    t_pre = time.time()
+    while time.time() - t_pre < 0.4:
+        step()
+        torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    clocks = sampler.stop()
+    pairs = B * w.Hq * sum(prefix + i + 1 for i in range(chunk))
+    tflops = 4.0 * pairs * w.D / (ms * 1e-3) / 1e12
+    peak, src = peak_tensor()
+    return {"metric": "prefill attention TFLOP/s (causal QK and PV, 4 D flop per query-key pair)",
+            "value": round(tflops, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": n,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": {0: "bf16", 4: "int4"}.get(mode, "fp8_e4m3"), "data": "synthetic",
+            "config": {"workload": desc, "mode": args.mode,
+                       "tokens_per_s": round(T / (ms * 1e-3), 1)},
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "kernel": "prefill_kernel (mma.sync f16, P split in two terms)",
+                         "peak_source": f"{src} bf16 dense"},
+            "gpu_launches": n, "clocks": clocks}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -712,10 +811,14 @@ def main(argv=None):
                     help="latency against context for BF16 / FP8 / FP8 + BF16 window layers / "
                          "INT4 instead of the throughput line")
     ap.add_argument("--sweep-contexts", default="1024,2048,4096,8192,16384,32768")
+    ap.add_argument("--prefill", action="store_true",
+                    help="prefill attention on the workload's chunk shape instead of the decode step")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     if args.latency_sweep:
         res = run_latency_sweep(args)
+    elif args.prefill:
+        res = run_prefill(args)
     else:
         res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
