@@ -270,10 +270,12 @@ struct Cfg {
 };
 
 // Resident CTAs per SM the register budget is sized for: four (16 warps,
-// <= 128 registers) where the accumulators fit without spilling, else two.
+// <= 128 registers) where the accumulators fit without spilling, three
+// (<= 168) for the eight-column split of GQA-8 at D = 128, else two.
 template <int MODE, int D, int G>
 struct MinCtas {
-  static constexpr int value = (D == 256 || (G == 8 && D >= 128) || (MODE == BF16 && G >= 4)) ? 2 : 4;
+  static constexpr int value =
+      (D == 256 || (MODE == BF16 && G >= 4)) ? 2 : ((G == 8 && D >= 128) ? 3 : 4);
 };
 
 // Shared memory: the warps' rings first (1024-aligned stages for the
