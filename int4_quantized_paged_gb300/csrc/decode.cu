@@ -286,9 +286,12 @@ struct Layout {
   static constexpr int q = G * D * 2;
   static constexpr int aux_of(int ns) { return (ns * C::SCALES + q + ns * 8 + 127) / 128 * 128; }
   static constexpr int warp_bytes(int ns) { return ns * C::STAGE + aux_of(ns); }
-  // Ring depth: the most stages (at most 6, at least PAIR + 1) with which
-  // MinCtas CTAs share the SM's 228 KB (1 KB per CTA is reserved by the
-  // system, 1 KB of each CTA's is alignment slack).
+  // Ring depth: two stages (one tile in flight per warp while one is
+  // computed keeps ~64 KB in flight per SM, enough for the copy bandwidth;
+  // deeper rings measured slower), three for the 4 KB tiles of quantized
+  // D = 256 layers; fewer if MinCtas CTAs would not share the SM's 228 KB
+  // (1 KB per CTA is reserved by the system, 1 KB of each CTA's is alignment
+  // slack).
   static constexpr int budget = 233472 / MinCtas<MODE, D, G>::value - 2048;
   static constexpr int fit(int ns) {
     return (ns > PAIR + 1 && WARPS * warp_bytes(ns) > budget) ? fit(ns - 1) : ns;
@@ -296,7 +299,7 @@ struct Layout {
 #ifdef KVQ_NS
   static constexpr int NS = KVQ_NS < PAIR + 1 ? PAIR + 1 : KVQ_NS;
 #else
-  static constexpr int NS = fit(6);
+  static constexpr int NS = fit((D == 256 && MODE != BF16) ? 3 : 2);
 #endif
   static constexpr int ring = NS * C::STAGE;
   static constexpr int scales = NS * C::SCALES;
@@ -789,11 +792,14 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
           if (whole || (p1 >= lo && p1 < L)) et_loc = max(et_loc, f32_exp(vsr[u][1]));
         }
       }
+      // score factors per accumulator element (row scale times column scale),
+      // formed apart from the QK result so they stay off its dependency chain
+      const float kq[4] = {kf0 * qc[0], kf0 * qc[1], kf1 * qc[0], kf1 * qc[1]};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int pos = pos0 + u * TILE + lg + ((e & 2) ? 8 : 0);
         const bool v = ok[u] && (whole || (pos >= lo && pos < L)) && (2 * lt + (e & 1)) < NCOL;
-        s_raw[u][e] = v ? sacc[u][e] * (e < 2 ? kf0 : kf1) * qc[e & 1] : -INFINITY;
+        s_raw[u][e] = v ? sacc[u][e] * kq[e] : -INFINITY;
       }
     }
 
