@@ -561,12 +561,24 @@ def cpu_baseline(args, mode: int, seconds: float = 10.0):
         oracle_step(st)
         steps += 1
     dt = (time.perf_counter() - t) / steps
+    # the same sample on one thread (two steps)
+    n_all = orc.num_threads()
+    orc.set_num_threads(1)
+    try:
+        t1 = time.perf_counter()
+        for _ in range(2):
+            oracle_step(st)
+        dt1 = (time.perf_counter() - t1) / 2
+    finally:
+        orc.set_num_threads(n_all)
     w = st["w"]
     return {"value": round(oracle_bytes(st) / dt / 1e9, 4), "unit": "GB/s",
-            "cores": orc.num_threads(), "kind": "oracle",
+            "cores": n_all, "kind": "oracle",
+            "value_one_thread": round(oracle_bytes(st) / dt1 / 1e9, 4),
             "sample": f"{w.B} of {wl_batch(args)} sequences x {st['n_kv']} of {w.Hkv} KV heads "
                       f"(their query heads, every layer) of the same decode step; {steps} timed "
-                      f"steps of {dt:.2f} s wall each"}
+                      f"steps of {dt:.2f} s wall each on {n_all} threads, 2 steps of "
+                      f"{dt1:.2f} s on one"}
 
 
 def wl_batch(args) -> int:
@@ -604,6 +616,23 @@ def run_reference(args):
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+def fit_line(points):
+    """Least-squares line y = a + b x through (x, y) points: (a, b)."""
+    n = len(points)
+    mx = sum(x for x, _ in points) / n
+    my = sum(y for _, y in points) / n
+    sxx = sum((x - mx) ** 2 for x, _ in points)
+    b = sum((x - mx) * (y - my) for x, y in points) / sxx if sxx > 0 else 0.0
+    return my - b * mx, b
+
+
+def break_even(a0, b0, a, b):
+    """Context where the line a + b x meets the reference a0 + b0 x (None if
+    they are parallel); below it the cheaper intercept wins, above it the
+    smaller slope."""
+    return None if b0 == b else (a - a0) / (b0 - b)
 
 
 def run_latency_sweep(args):
@@ -666,15 +695,7 @@ def run_latency_sweep(args):
             del st, graph
             torch.cuda.empty_cache()
 
-    def fit(pts):
-        n = len(pts)
-        mx = sum(x for x, _ in pts) / n
-        my = sum(y for _, y in pts) / n
-        sxx = sum((x - mx) ** 2 for x, _ in pts)
-        b = sum((x - mx) * (y - my) for x, y in pts) / sxx if sxx > 0 else 0.0
-        return my - b * mx, b
-
-    lines = {name: fit(p) for name, p in points.items()}
+    lines = {name: fit_line(p) for name, p in points.items()}
     a0, b0 = lines["bf16"]
     res = {"metric": "decode-step latency vs context (fitted ms per context token; break-even "
                      "context vs BF16)",
@@ -684,7 +705,8 @@ def run_latency_sweep(args):
         v = {"ms": [round(y, 4) for _, y in points[name]], "intercept_ms": round(a, 5),
              "slope_ms_per_token": float("%.4g" % b)}
         if name != "bf16":
-            v["break_even_context"] = (round((a - a0) / (b0 - b), 1) if b0 != b else None)
+            be = break_even(a0, b0, a, b)
+            v["break_even_context"] = None if be is None else round(be, 1)
         res["variants"][name] = v
     return res
 

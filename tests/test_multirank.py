@@ -73,3 +73,13 @@ def test_byte_accounting_matches_the_pages_per_token_formulas():
     # write bytes per token: Hkv x (bf16 K+V in + codes out + scales) + int64 slot
     assert bench.write_bytes(w, 3, 1) == 8 * (4 * 128 + 2 * 128 + 8) + 8 == 6216
     assert bench.write_bytes(w, 4, 1) == 8 * (4 * 128 + 128 + 8) + 8
+
+
+def test_latency_sweep_line_fit_and_break_even():
+    import bench
+    pts = [(1024, 0.5 + 2e-5 * 1024), (4096, 0.5 + 2e-5 * 4096), (32768, 0.5 + 2e-5 * 32768)]
+    a, b = bench.fit_line(pts)
+    assert abs(a - 0.5) < 1e-12 and abs(b - 2e-5) < 1e-15
+    # quantized line: higher intercept, lower slope -> meets BF16 at (0.6 - 0.5) / (3e-5 - 2e-5)
+    assert abs(bench.break_even(0.5, 3e-5, 0.6, 2e-5) - 10000.0) < 1e-6
+    assert bench.break_even(0.5, 2e-5, 0.6, 2e-5) is None
