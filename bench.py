@@ -280,10 +280,11 @@ def setup_gpu(args, dev, rank, w=None, time_fill=True):
     return dict(w=w, L=L, pg=pg, ctx=ctx, layers=layers, slots_new=slots_new, fill=fill_ms)
 
 
-def launch_layer(st, li, ev=None, stream=None, inputs=None):
+def launch_layer(st, li, ev=None, stream=None, inputs=None, out=None):
     """One layer of the decode step: write the current token, then decode."""
     from int4_quantized_paged_gb300 import kvq
     lay = st["layers"][li]
+    out = lay["out"] if out is None else out
     q, kn, vn, sl, bt, cl = inputs if inputs is not None else (
         lay["q"], lay["k_new"], lay["v_new"], st["slots_new"], st["pg"].block_table,
         st["pg"].context_lens)
@@ -293,7 +294,7 @@ def launch_layer(st, li, ev=None, stream=None, inputs=None):
                         lay["k_scale"], lay["v_scale"])
     if ev is not None:
         ev[1].record(stream)
-    kvq.kvq_decode_attention(st["ctx"], li, q, lay["kc"], lay["vc"], bt, cl, lay["out"],
+    kvq.kvq_decode_attention(st["ctx"], li, q, lay["kc"], lay["vc"], bt, cl, out,
                              max_context=st["L"], k_scale=lay["k_scale"], v_scale=lay["v_scale"],
                              k_cache_scale=lay["ks"], v_cache_scale=lay["vs"],
                              num_workers=lay["workers"], workspace=lay["ws"])
@@ -382,27 +383,42 @@ def run_gpu(args):
     if kvq.kvq_get_device_error() != 0:
         raise RuntimeError("device error word set during the timed steps")
 
-    # end to end through the C ABI with host buffers (un-graphed calls)
-    pin = lambda t: t.cpu().pin_memory()
-    shared = [st["slots_new"], st["pg"].block_table, st["pg"].context_lens]
-    h_in = [[pin(lay[k]) for k in ("q", "k_new", "v_new")] for lay in layers]
-    h_sh = [pin(x) for x in shared]
-    d_in = [[torch.empty_like(x, device=dev) for x in row] for row in h_in]
-    d_sh = [torch.empty_like(x, device=dev) for x in h_sh]
-    h_out = [torch.empty(lay["out"].shape, dtype=torch.float32).pin_memory() for lay in layers]
-    h2d = sum(x.numel() * x.element_size() for row in h_in for x in row) + \
-        sum(x.numel() * x.element_size() for x in h_sh)
-    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    # end to end through the C ABI with host buffers (un-graphed calls): the
+    # step's inputs travel in one pinned staging buffer (one host-to-device
+    # copy) and its outputs come back in one (one device-to-host copy); the
+    # kernels read and write views of the device-side buffers
+    def layout(tensors):
+        offs, total = [], 0
+        for t in tensors:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, total
+
+    in_t = [st["slots_new"], st["pg"].block_table, st["pg"].context_lens] + \
+        [lay[k] for lay in layers for k in ("q", "k_new", "v_new")]
+    offs, total_in = layout(in_t)
+    h_in = torch.empty(total_in, dtype=torch.uint8).pin_memory()
+    for t, o in zip(in_t, offs):
+        nb = t.numel() * t.element_size()
+        h_in[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+    d_in = torch.empty(total_in, dtype=torch.uint8, device=dev)
+    dv = [d_in[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+          for t, o in zip(in_t, offs)]
+    out_t = [lay["out"] for lay in layers]
+    ooffs, total_out = layout(out_t)
+    d_out = torch.empty(total_out, dtype=torch.uint8, device=dev)
+    ov = [d_out[o:o + t.numel() * 4].view(torch.float32).view(t.shape)
+          for t, o in zip(out_t, ooffs)]
+    h_out = torch.empty(total_out, dtype=torch.uint8).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in in_t)
+    d2h = sum(t.numel() * t.element_size() for t in out_t)
 
     def e2e_step():
-        for d, h in zip(d_sh, h_sh):
-            d.copy_(h, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         for li in range(nl):
-            for d, h in zip(d_in[li], h_in[li]):
-                d.copy_(h, non_blocking=True)
-            launch_layer(st, li, inputs=(d_in[li][0], d_in[li][1], d_in[li][2], d_sh[0],
-                                         d_sh[1], d_sh[2]))
-            h_out[li].copy_(layers[li]["out"], non_blocking=True)
+            q, kn, vn = dv[3 + 3 * li:6 + 3 * li]
+            launch_layer(st, li, inputs=(q, kn, vn, dv[0], dv[1], dv[2]), out=ov[li])
+        h_out.copy_(d_out, non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()

@@ -317,6 +317,15 @@ kvq_status decode_impl(const kvq_ctx* ctx, int layer, const void* q, const float
   a.workers = workers;
   a.num_blocks = c.num_blocks;
   a.qk_scale = ctx->softmax_scale * 1.4426950408889634f;
+  {
+    // upper bound of the cache bytes this call reads; beyond ~half the L2 the
+    // pages cannot survive to the next step, so they are streamed evict-first
+    const long long win = ctx->window[layer];
+    const long long pos = (win > 0 && win < max_context) ? win : max_context;
+    const double bytes = (double)batch * c.num_kv_heads * (double)pos *
+                         (2.0 * (double)row_bytes(mode, c.head_dim) + (is_dynamic(mode) ? 8 : 0));
+    a.stream_once = bytes > 64.0 * 1024 * 1024;
+  }
   return cuda_status(
       kvq::launch_decode(mode, c.head_dim, G, a, static_cast<cudaStream_t>(stream)));
 }

@@ -508,6 +508,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
   mbar_init_fence();
   __syncwarp();
 
+  const uint64_t l2_policy = l2_copy_policy(a.stream_once != 0);
   unsigned valid_mask = 0;        // bit s: stage s holds a fetched tile
   int pst = 0;                    // stage the next issued tile goes to
   // Block id of the producer cursor's tile, loaded one issue ahead so that its
@@ -531,8 +532,9 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
         uint64_t* bar = &wbars[st];
         mbar_expect_tx(bar, 2 * C::TB + C::SCALES);
         uint8_t* kd = wcodes + st * C::STAGE;
-        tma_tile_2d(kd, &kmap, 0, row, bar);
-        tma_tile_2d(kd + C::TBP, &vmap, 0, row, bar);
+        // a layer whose pages cannot stay in L2 streams them evict-first
+        tma_tile_2d_hint(kd, &kmap, 0, row, bar, l2_policy);
+        tma_tile_2d_hint(kd + C::TBP, &vmap, 0, row, bar, l2_policy);
         if constexpr (C::DYN) {
           bulk_copy(wscales + st * 32, a.k_cs + cell, 64, bar);
           bulk_copy(wscales + st * 32 + 16, a.v_cs + cell, 64, bar);

@@ -52,6 +52,7 @@ struct DecodeArgs {
   long long* item_tiles;       // [B*Hkv + 1] first tile of each item in the tile list; T last
   unsigned* err;
   int B, Hq, Hkv, bs, bs_shift, max_blocks, window, workers;
+  int stream_once;             // pages larger than L2: copy them evict-first
   long long num_blocks;
   float qk_scale;              // softmax_scale * log2(e)
 };

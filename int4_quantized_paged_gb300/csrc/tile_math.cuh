@@ -26,6 +26,28 @@ __device__ __forceinline__ void tma_tile_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// As tma_tile_2d, with an L2 eviction-priority policy (createpolicy) for
+// data read once.
+__device__ __forceinline__ void tma_tile_2d_hint(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for copies: evict first (data streamed once, larger than L2) or
+// normal priority (data that may still be in L2 at its next use).
+__device__ __forceinline__ uint64_t l2_copy_policy(bool evict_first) {
+  uint64_t pol;
+  if (evict_first)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // Four E4M3 codes (one word) -> two f16x2: bytes 0,1 -> lo; bytes 2,3 -> hi.
 // The conversion is exact.
 __device__ __forceinline__ void e4m3x4_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
