@@ -83,3 +83,19 @@ def test_latency_sweep_line_fit_and_break_even():
     # quantized line: higher intercept, lower slope -> meets BF16 at (0.6 - 0.5) / (3e-5 - 2e-5)
     assert abs(bench.break_even(0.5, 3e-5, 0.6, 2e-5) - 10000.0) < 1e-6
     assert bench.break_even(0.5, 2e-5, 0.6, 2e-5) is None
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    """bench.py --impl reference runs the oracle on host cores and prints one
+    JSON line with the keys the benchmark contract names."""
+    import json
+    import bench
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--cpu-seqs", "1"])
+    line = capsys.readouterr().out.strip().splitlines()[-1]
+    d = json.loads(line)
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
