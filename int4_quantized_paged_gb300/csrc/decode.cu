@@ -20,21 +20,26 @@
 //    runs across item boundaries.  For each item segment it covers, a warp
 //    either writes the final output (it covered the whole item) or a partial
 //    (running max m, sum l, unnormalised O) that a merge kernel combines by
-//    log-sum-exp.  Warps never wait on one another.
+//    log-sum-exp; the merge is a programmatic dependent launch, so its launch
+//    overlaps this grid's tail.  Warps never wait on one another.
 //  * Each warp streams its tiles through an NS-stage ring in shared memory
 //    with TMA: a 2-D tensor copy each for the K and V code tile (128-byte
 //    rows, 128B swizzle so the fragment loads below hit no bank conflicts)
 //    and, for dynamic scales, a 64-byte bulk copy each of the tile's K and V
 //    scales, completing on the stage's mbarrier.  The copies of the next
 //    NS-1 tiles (of this or the next item) are in flight while one tile is
-//    computed.  Every wait is bounded: a wait that runs out sets the TIMEOUT
-//    bit of the device error word, drains the warp's copies and stops.
+//    computed.  Pages of a layer larger than L2 are copied evict-first.
+//    Every wait is bounded: a wait that runs out sets the TIMEOUT bit of the
+//    device error word, drains the warp's copies and stops.
 //  * QK on tensor cores: S^T[16 positions x 8 columns] = K_tile . Q^T with
 //    mma.m16n8k16, fp32 accumulate.  E4M3 and INT4 codes convert exactly to
-//    f16; q (bf16) times a power of two converts exactly to f16.  Columns
-//    are the G query heads of the KV head.
+//    f16; q (bf16) times a power of two converts exactly to f16 (an FP8
+//    query's E4M3 values are f16 values).  Columns are the G query heads of
+//    the KV head, repeated once per term of the weight split when they fit
+//    in the 8 columns, so a QK column is already the PV column it feeds.
 //  * Online softmax in log2 units on the fragments (running max over the raw
-//    scores).  The weights that meet V are P' = p * v_scale * 2^k, with k a
+//    scores, reduced over the warp only on tiles where some lane holds a
+//    larger score).  The weights that meet V are P' = p * v_scale * 2^k, with k a
 //    power-of-two range factor that keeps P' below 2^14, so both f16 terms of
 //    its split stay normal numbers.
 //  * PV on tensor cores with d as the M dimension: O^T[d x cols] += V^T P'.
@@ -42,6 +47,8 @@
 //    terms for BF16 layers) so the weighted sum keeps fp32-class accuracy;
 //    for G*terms <= 8 all terms share one 8-column tile.  The P' fragment
 //    comes from the S^T fragment by movmatrix (in-register 8x8 transpose).
+//  * Outputs are fp32, or their round-to-nearest-even bf16 for the bf16
+//    variant.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -55,11 +62,14 @@ namespace kvq {
 namespace {
 
 constexpr int WARPS = 4;         // worker warps per CTA (independent)
+// Tuning knobs (build-time): tiles per loop iteration (1 measured best; 2
+// shares the softmax reductions between two tiles at the cost of registers)
+// and the QK accumulator chains (2 shortens the MMA dependency chain).
 #ifndef KVQ_TILES_PER_ITER
 #define KVQ_TILES_PER_ITER 1
 #endif
 #ifndef KVQ_QK2
-#define KVQ_QK2 1              // two independent QK accumulator chains
+#define KVQ_QK2 1
 #endif
 constexpr int PAIR = KVQ_TILES_PER_ITER;   // 16-position tiles per loop iteration
 constexpr int TILE = 16;         // positions per tile
