@@ -8,6 +8,11 @@
  *   kvq_decode_attention  paged GQA decode over that cache, K scale folded
  *                         into the QK product, V scale into the PV sum.
  *
+ * Around them: the work plan of the decode (kvq_decode_plan), its variants
+ * (bf16 output, FP8 query, no caller workspace), prefill attention over the
+ * same cache (kvq_prefill_attention), static per-head calibration, the
+ * capacity accounting of the pages and the device codec on its own.
+ *
  * The operations and their scale layouts follow three pages:
  *   [P1] "Per-tensor vs per-head FP8 KV cache scales"
  *   [P2] "Per-token-head KV cache scale overhead"

@@ -8,9 +8,11 @@ arithmetic, written from the same layout contract.
 
 Parity pinned: the codec (exhaustive and against the printed E4M3 format and
 torch's float8 cast), the write (amax invariant, zero-vector rule, skipped
-slots, plain-cast special case, closed-form error bound) and the decode
-(library softmax attention for BF16 layers, L = 1, K = 0, window >= L) are all
-checked against facts that do not come from this module; see tests/.
+slots, plain-cast special case, closed-form error bound), the decode
+(library softmax attention for BF16 layers, L = 1, K = 0, window >= L), the
+prefill (masked library attention, causal and window) and the FP8 query
+(torch's E4M3 cast, ties and saturation) are all checked against facts that
+do not come from this module; see tests/.
 """
 from __future__ import annotations
 
