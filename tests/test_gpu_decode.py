@@ -196,3 +196,18 @@ def test_window_layer_ring_reuse_of_blocks(mode):
                         k_scale=r.o_k_scale, v_scale=r.o_v_scale)
     r.host = (kc, vc, ks, vs)
     r.check_decode(outs["ring"], where=f"ring mode {mode}")
+
+
+@pytest.mark.parametrize("mode", [orc.FP8_PER_TOKEN_HEAD, orc.BF16])
+@pytest.mark.parametrize("workers", [7, 0])
+def test_batch_above_128_sequences(mode, workers):
+    """More than 128 sequences: warps find their share by the two-pass scan
+    rather than the single round of context-length loads."""
+    rng = np.random.default_rng(17)
+    lens = tuple(int(x) for x in rng.integers(0, 200, size=150))
+    w = wl.Workload("wide", Hq=4, Hkv=2, D=64, block_size=16, context_lens=lens, windows=(0,),
+                    head_mult=(1.0, 16.0), outlier_p=0.05, outlier_factor=4.0, seed=83)
+    r = LayerRun(w, mode)
+    r.write()
+    out = r.decode(num_workers=workers)
+    r.check_decode(out, where=f"wide batch mode {mode} workers {r.workers}")
