@@ -10,7 +10,11 @@ prefill-shaped cache write of the whole 262,144-token context (cache-write
 GB/s).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--mode fp8_per_token_head]
+                    [--workload llama8b|llama70b_128k|gptoss20b|gemma_d256]
+                    [--skip-sliding] [--workers N] [--graph | --no-graph]
     python bench.py --impl reference     # the CPU oracle on a bounded sample
+    python bench.py --prefill --workload llama8b|gemma_d256     # prefill TFLOP/s
+    python bench.py --latency-sweep --workload gptoss20b        # latency vs context
 
 Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
 work shards by sequence with no exchange); rank 0 prints the line.
