@@ -211,3 +211,14 @@ def test_batch_above_128_sequences(mode, workers):
     r.write()
     out = r.decode(num_workers=workers)
     r.check_decode(out, where=f"wide batch mode {mode} workers {r.workers}")
+
+
+@pytest.mark.parametrize("scale", [0.03, 2.5])
+def test_per_tensor_scale_other_than_one(scale):
+    """The per-tensor path with K and V scales that are not 1: the scale enters
+    the write's division, the decode's score factor and its unscale."""
+    w = SMALL["llama8b"]
+    r = LayerRun(w, orc.FP8_PER_TENSOR, per_tensor_scale=scale)
+    r.write()
+    r.check_write()
+    r.check_decode(r.decode(num_workers=0), where=f"per-tensor scale {scale}")
