@@ -99,3 +99,22 @@ def test_reference_arm_prints_the_contract_line(capsys):
         assert k in d, k
     assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched as two ranks (the N > 1 form), the reference arm runs on rank 0
+    only and prints exactly one line; the other rank exits 0."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", "29531", "bench.py", "--gpus", "2",
+           "--impl", "reference", "--steps", "1", "--warmup", "3", "--cpu-seqs", "1"]
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
