@@ -97,6 +97,11 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_ctx** out) {
     const int m = cfg->layer_mode[l];
     if (m < KVQ_BF16 || m > KVQ_INT4_PER_TOKEN_HEAD) return KVQ_ERR_INVALID_ARG;
     if (!kvq::decode_supported(m, cfg->head_dim, G)) return KVQ_ERR_UNSUPPORTED;
+    // TMA addresses the code buffer in 128-byte rows with a signed 32-bit
+    // coordinate
+    if (cfg->num_blocks * (long long)cfg->num_kv_heads * bs * row_bytes(m, cfg->head_dim) / 128 >=
+        (1LL << 31))
+      return KVQ_ERR_UNSUPPORTED;
     if (cfg->layer_window && cfg->layer_window[l] < 0) return KVQ_ERR_INVALID_ARG;
   }
   kvq_ctx* c = new (std::nothrow) kvq_ctx;

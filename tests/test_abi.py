@@ -49,6 +49,11 @@ def test_create_validates_config():
         _ctx([3], windows=[-1])
     with pytest.raises(kvq.KVQError, match="UNSUPPORTED"):
         _ctx([3], Hq=96, Hkv=4)      # GQA ratio 24 not built
+    # a BF16 D=256 layer of 2^30 cells spans 2^32 rows of 128 bytes: past the
+    # signed 32-bit TMA coordinate; the same pool in FP8 D=128 spans 2^30
+    with pytest.raises(kvq.KVQError, match="UNSUPPORTED"):
+        _ctx([0], Hq=16, Hkv=8, D=256, nb=1 << 23)
+    _ctx([3], Hq=16, Hkv=8, D=128, nb=1 << 23)
 
 
 def test_layer_buffer_sizes():
