@@ -7,9 +7,12 @@
 // overhead", section "INT4 makes the metadata fraction larger".
 //
 // The write is a pure HBM stream: per token and KV head it reads 2*2D bytes
-// of bf16 K/V and writes 2*D*elem code bytes plus 8 scale bytes.  One group of
-// D/8 lanes owns one head vector (16-byte loads, 8 bf16 per lane); the amax is
-// a shuffle reduction inside the group.
+// of bf16 K/V and writes 2*D*elem code bytes plus 8 scale bytes.  Two kernels
+// share the arithmetic: write_staged_kernel for large writes (token rows
+// streamed into a shared-memory ring by bulk copies; one group of D/16 lanes
+// per head vector) and write_kernel for small writes and BF16 layers (one
+// group of D/8 lanes per vector, 16-byte loads straight into registers).  In
+// both the amax is a shuffle reduction inside the group.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
