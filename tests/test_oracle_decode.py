@@ -160,3 +160,29 @@ def test_empty_context_gives_zeros_and_pairs_subset_matches_full():
     sub = orc.decode(orc.FP8_PER_TOKEN_HEAD, q, kc, vc, fill["block_table"], cl,
                      k_cache_scale=ks, v_cache_scale=vs, pairs=pairs)
     assert np.array_equal(sub[0], full[1, 3]) and np.array_equal(sub[1], full[1, 0])
+
+
+@pytest.mark.parametrize("bs", [32, 64, 128])
+@pytest.mark.parametrize("mode", [orc.FP8_PER_TOKEN_HEAD, orc.INT4_PER_TOKEN_HEAD, orc.BF16])
+def test_decode_and_prefill_do_not_depend_on_the_page_size(bs, mode):
+    """The same tokens paged in 16-position blocks and in larger ones give the
+    same attention: the page size only moves where a position is stored."""
+    import dataclasses
+    outs = {}
+    for size in (16, bs):
+        w = dataclasses.replace(TINY, block_size=size)
+        fill = host_fill(w)
+        kc, vc, ks, vs = orc.alloc_cache(mode, fill["paging"].num_blocks, w.Hkv, size, w.D)
+        orc.cache_write(mode, fill["k_bits"], fill["v_bits"], fill["slots_np"], kc, vc, ks, vs,
+                        block_size=size)
+        q = bits(wl.queries(w, "cpu"))
+        dec = orc.decode(mode, q, kc, vc, fill["block_table"], fill["context_lens"],
+                         k_cache_scale=ks, v_cache_scale=vs, window=20, block_size=size)
+        qs = np.array([0, 10, 60], dtype=np.int32)
+        qp = bits(wl.kv_tokens(w, 60, "cpu", stream_base=703)[0][:, :1].expand(-1, w.Hq, -1)
+                  .contiguous())
+        pre = orc.prefill(mode, qp, kc, vc, fill["block_table"], qs, fill["context_lens"],
+                          k_cache_scale=ks, v_cache_scale=vs, block_size=size)
+        outs[size] = (dec, pre)
+    assert np.array_equal(outs[16][0], outs[bs][0])
+    assert np.array_equal(outs[16][1], outs[bs][1])
