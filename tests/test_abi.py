@@ -174,3 +174,40 @@ def test_bf16_output_decode_validates_like_fp32():
 def test_status_strings():
     for s in range(8):
         assert kvq.kvq_status_string(s)
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """include/kvq.h compiles as C99 with warnings as errors, and a C program
+    using only host-side calls links against libkvq.so and runs."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lib_dir = os.path.dirname(kvq.LIB_PATH)
+    lib_name = os.path.basename(kvq.LIB_PATH)
+    src = tmp_path / "use_kvq.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "kvq.h"
+int main(void) {
+  int modes[2] = {KVQ_FP8_PER_TOKEN_HEAD, KVQ_BF16};
+  int windows[2] = {0, 128};
+  kvq_config cfg = {2, 32, 8, 128, 16, 1024, modes, windows, 0.0f};
+  kvq_ctx* ctx = NULL;
+  kvq_status st = kvq_create(&cfg, &ctx);
+  if (st != KVQ_OK) { printf("create: %s\n", kvq_status_string(st)); return 1; }
+  size_t code = 0, scale = 0;
+  st = kvq_layer_buffer_sizes(ctx, 0, &code, &scale);
+  printf("%d %zu %zu\n", (int)st, code, scale);
+  kvq_destroy(ctx);
+  return st == KVQ_OK && code == 1024u * 8u * 16u * 128u && scale == 1024u * 8u * 16u * 4u ? 0 : 2;
+}
+''')
+    exe = tmp_path / "use_kvq"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I",
+                        os.path.join(ROOT, "include"), str(src), "-L", lib_dir, "-l:" + lib_name,
+                        "-Wl,-rpath," + lib_dir, "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
