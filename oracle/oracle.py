@@ -8,7 +8,8 @@ arithmetic, written from the same layout contract.
 
 Parity pinned: the codec (exhaustive and against the printed E4M3 format and
 torch's float8 cast), the write (amax invariant, zero-vector rule, skipped
-slots, plain-cast special case, closed-form error bound), the decode
+slots, plain-cast special case, closed-form error bound, hand-worked bytes
+of INT4 packing and FP8 codes), the decode
 (library softmax attention for BF16 layers, L = 1, K = 0, window >= L), the
 prefill (masked library attention, causal and window) and the FP8 query
 (torch's E4M3 cast, ties and saturation) are all checked against facts that

@@ -194,3 +194,49 @@ def test_calibration_is_per_head_amax_over_448():
     got = orc.calibrate_per_head(xb)
     amax = np.abs(bf16_to_f64(xb)).max(axis=(0, 2)).astype(np.float32)
     assert np.array_equal(got, amax / np.float32(448.0))
+
+
+def _one_vector(mode, values, D=64):
+    """Writes one token (one KV head) whose first elements are `values` (the
+    rest zero) to slot 0 and returns its code row and scale."""
+    x = torch.zeros((1, 1, D), dtype=torch.bfloat16)
+    x[0, 0, :len(values)] = torch.tensor(values, dtype=torch.float64).to(torch.bfloat16)
+    xb = bits(x)
+    kc, vc, ks, vs = orc.alloc_cache(mode, 1, 1, 16, D)
+    orc.cache_write(mode, xb, xb, np.zeros(1, dtype=np.int64), kc, vc, ks, vs)
+    assert np.array_equal(kc, vc) and np.array_equal(ks, vs)
+    return kc[0, 0, 0], ks[0, 0, 0]
+
+
+def test_int4_packing_hand_computed_bytes():
+    """Packed INT4 ("Per-token-head KV cache scale overhead", section "INT4
+    makes the metadata fraction larger": widths halved, two values a byte),
+    read as two's-complement nibbles with the even element in the low
+    nibble.  The bytes below are worked out by hand, not by the oracle."""
+    # amax 7 -> scale 1: the codes are the values themselves, -7..7 then -7
+    row, s = _one_vector(orc.INT4_PER_TOKEN_HEAD,
+                         [-7, -6, -5, -4, -3, -2, -1, 0, 1, 2, 3, 4, 5, 6, 7, -7])
+    assert s == 1.0
+    assert list(row[:8]) == [0xA9, 0xCB, 0xED, 0x0F, 0x21, 0x43, 0x65, 0x97]
+    assert not row[8:].any()
+    # amax 14 -> scale 2: 14/2 = 7, -3/2 = -1.5 -> -2, 5/2 = 2.5 -> 2 (ties to
+    # even), 1/2 = 0.5 -> 0, -13/2 = -6.5 -> -6, 9/2 = 4.5 -> 4
+    row, s = _one_vector(orc.INT4_PER_TOKEN_HEAD, [14, -3, 5, 1, -13, 9])
+    assert s == 2.0
+    assert list(row[:3]) == [0xE7, 0x02, 0x4A]
+    assert not row[3:].any()
+
+
+def test_fp8_dynamic_hand_computed_codes():
+    """Dynamic FP8: scale = amax/448 in fp32, codes are E4M3 of x/scale
+    ("Per-tensor vs per-head FP8 KV cache scales", section "Dynamic
+    per-token-head scales add 3.125 percent").  amax 448 gives scale 1, so
+    the codes are the E4M3 encodings of the values, worked out by hand:
+    448 = 1.75 x 2^8 -> 0x7E; -224 = -1.75 x 2^7 -> 0xF6; 1 -> 0x38;
+    0.3125 = 1.25 x 2^-2 -> 0x2A; 2^-9 (smallest subnormal) -> 0x01;
+    -17 lies halfway between -16 and -18 (spacing 2 at 2^4) and takes the even
+    mantissa, -16 = -1.0 x 2^4 -> 0xD8."""
+    row, s = _one_vector(orc.FP8_PER_TOKEN_HEAD, [448, -224, 1, 0.3125, 2.0 ** -9, -17])
+    assert s == 1.0
+    assert list(row[:6]) == [0x7E, 0xF6, 0x38, 0x2A, 0x01, 0xD8]
+    assert not row[6:].any()
