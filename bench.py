@@ -110,16 +110,43 @@ def write_bytes(w, mode: int, T: int) -> float:
     return T * (w.Hkv * (4 * w.D + 2 * w.D * elem_bytes(mode) + (8 if dyn else 0)) + 8)
 
 
-def peak_hbm():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def measured_peak(names, path=None):
+    """First positive number stored under one of `names` anywhere in the
+    measured-peaks file (top level or nested), else None."""
+    path = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
-        d = json.load(open(p))
-        v = d.get("hbm_gbs") or d.get("hbm_GBps")
-        if v:
-            return float(v), "measured"
-    except Exception:
-        pass
-    return FALLBACK_HBM_GBS, "fallback"
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+
+    def find(node, name):
+        if isinstance(node, dict):
+            v = node.get(name)
+            if isinstance(v, (int, float)) and not isinstance(v, bool) and v > 0:
+                return float(v)
+            for child in node.values():
+                r = find(child, name)
+                if r is not None:
+                    return r
+        elif isinstance(node, list):
+            for child in node:
+                r = find(child, name)
+                if r is not None:
+                    return r
+        return None
+
+    for name in names:
+        r = find(d, name)
+        if r is not None:
+            return r
+    return None
+
+
+def peak_hbm(path=None):
+    """HBM copy bandwidth (GB/s) and its source."""
+    v = measured_peak(("hbm_gbs", "hbm_GBps"), path)
+    return (v, "measured") if v else (FALLBACK_HBM_GBS, "fallback")
 
 
 def profiled_traffic(kernel_file: str, summary: str):
@@ -739,17 +766,11 @@ PREFILL = {
 }
 
 
-def peak_tensor():
-    """Dense bf16 tensor peak (TFLOP/s) and its source."""
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            d = json.load(f)
-        for k in ("bf16_tflops", "bf16_dense_tflops"):
-            if k in d:
-                return float(d[k]), "measured"
-    except (OSError, ValueError):
-        pass
-    return 1900.0, "fallback"
+def peak_tensor(path=None):
+    """Dense bf16 tensor peak (TFLOP/s, the burst figure: the prefill kernel
+    is timed alone) and its source."""
+    v = measured_peak(("bf16_tflops", "bf16_dense_tflops"), path)
+    return (v, "measured") if v else (1900.0, "fallback")
 
 
 def run_prefill(args):

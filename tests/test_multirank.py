@@ -4,6 +4,7 @@ The path shards by sequence (replicas only, no data-path collective); what
 the ranks share is the timing protocol: a barrier around the timed region,
 the maximum of the ranks' step times and the sum of their bytes.
 """
+import json
 import os
 import socket
 
@@ -118,3 +119,23 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+def test_measured_peaks_read_flat_or_nested(tmp_path):
+    """The roofline denominators come from the measured-peaks file whether
+    its figures sit at the top level or inside a nested object; a missing or
+    unreadable file falls back and says so."""
+    flat = tmp_path / "flat.json"
+    flat.write_text(json.dumps({"hbm_gbs": 6784.5, "bf16_tflops": 1936.0,
+                                "bf16_tflops_sustained": 1700.0}))
+    assert bench.peak_hbm(str(flat)) == (6784.5, "measured")
+    assert bench.peak_tensor(str(flat)) == (1936.0, "measured")
+    nested = tmp_path / "nested.json"
+    nested.write_text(json.dumps({"gpu": "GB300", "peaks": {"hbm_gbs": 6700, "bf16_tflops": 1900.5}}))
+    assert bench.peak_hbm(str(nested)) == (6700.0, "measured")
+    assert bench.peak_tensor(str(nested)) == (1900.5, "measured")
+    bad = tmp_path / "bad.json"
+    bad.write_text("{not json")
+    assert bench.peak_hbm(str(bad)) == (bench.FALLBACK_HBM_GBS, "fallback")
+    assert bench.peak_hbm(str(tmp_path / "absent.json"))[1] == "fallback"
+    assert bench.peak_tensor(str(tmp_path / "absent.json")) == (1900.0, "fallback")
