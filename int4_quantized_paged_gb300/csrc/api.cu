@@ -107,11 +107,16 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_ctx** out) {
   kvq_ctx* c = new (std::nothrow) kvq_ctx;
   if (!c) return KVQ_ERR_INVALID_ARG;
   c->cfg = *cfg;
-  c->mode.assign(cfg->layer_mode, cfg->layer_mode + cfg->num_layers);
-  if (cfg->layer_window)
-    c->window.assign(cfg->layer_window, cfg->layer_window + cfg->num_layers);
-  else
-    c->window.assign(cfg->num_layers, 0);
+  try {  // no exception may cross the C ABI
+    c->mode.assign(cfg->layer_mode, cfg->layer_mode + cfg->num_layers);
+    if (cfg->layer_window)
+      c->window.assign(cfg->layer_window, cfg->layer_window + cfg->num_layers);
+    else
+      c->window.assign(cfg->num_layers, 0);
+  } catch (...) {
+    delete c;
+    return KVQ_ERR_INVALID_ARG;
+  }
   c->cfg.layer_mode = c->mode.data();
   c->cfg.layer_window = c->window.data();
   c->softmax_scale =
