@@ -333,6 +333,19 @@ def launch_layer(st, li, ev=None, stream=None, inputs=None, out=None):
         ev[2].record(stream)
 
 
+def layer_breakdown(layers, dbytes, dec_ms, write_ms):
+    """Per-layer times of the step (mean CUDA-event ms of each layer's write
+    and decode + merge) and the decode's algorithmic GB/s, layers in order."""
+    out = []
+    for li, lay in enumerate(layers):
+        d = statistics.mean(dec_ms[li])
+        out.append({"layer": li, "mode": int(lay["mode"]), "window": int(lay["window"]),
+                    "decode_ms": round(d, 5),
+                    "decode_gbs": round(dbytes[li] / (d * 1e-3) / 1e9, 2) if d > 0 else None,
+                    "write_ms": round(statistics.mean(write_ms[li]), 5)})
+    return out
+
+
 def run_gpu(args):
     import torch
     from int4_quantized_paged_gb300 import kvq
@@ -516,6 +529,7 @@ def run_gpu(args):
         "e2e": {"value": round(all_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
+        "layers": layer_breakdown(layers, dbytes, dec_ms, write_ms),
         "gpu_launches": 3 * nl * n,
         "clocks": clocks,
     }

@@ -139,3 +139,17 @@ def test_measured_peaks_read_flat_or_nested(tmp_path):
     assert bench.peak_hbm(str(bad)) == (bench.FALLBACK_HBM_GBS, "fallback")
     assert bench.peak_hbm(str(tmp_path / "absent.json"))[1] == "fallback"
     assert bench.peak_tensor(str(tmp_path / "absent.json")) == (1900.0, "fallback")
+
+
+def test_layer_breakdown_reports_every_layer():
+    """Per-layer decode and write times (a two-layer window / full pair)."""
+    layers = [{"mode": 3, "window": 512}, {"mode": 3, "window": 0}]
+    dbytes = [68.2e6, 2.18e9]
+    dec_ms = [[0.02, 0.02], [0.33, 0.35]]
+    write_ms = [[0.008], [0.009]]
+    rows = bench.layer_breakdown(layers, dbytes, dec_ms, write_ms)
+    assert [r["layer"] for r in rows] == [0, 1]
+    assert [r["window"] for r in rows] == [512, 0]
+    assert rows[0]["decode_gbs"] == round(68.2e6 / 0.02e-3 / 1e9, 2)
+    assert rows[1]["decode_ms"] == 0.34 and rows[1]["write_ms"] == 0.009
+    json.dumps(rows)
