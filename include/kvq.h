@@ -157,6 +157,12 @@ kvq_status kvq_calibrate_per_head(const kvq_ctx* ctx, const void* x, long long n
 kvq_status kvq_decode_plan(const kvq_ctx* ctx, int layer, int batch, int max_context,
                            int* num_workers, size_t* workspace_bytes);
 
+/* Workspace bytes of a decode call with num_workers = 0 (the plan's choice):
+ * kvq_decode_plan's *workspace_bytes for that count.  0 when one worker
+ * suffices, and also when an argument is invalid (kvq_decode_plan reports
+ * which). */
+size_t kvq_decode_workspace_size(const kvq_ctx* ctx, int layer, int batch, int max_context);
+
 /* Paged decode attention, one query token per sequence.
  *
  * q: bf16 [batch][Hq][D], 16-byte aligned.  Query head hq reads KV head

@@ -250,6 +250,13 @@ kvq_status kvq_decode_plan(const kvq_ctx* ctx, int layer, int batch, int max_con
   return KVQ_OK;
 }
 
+size_t kvq_decode_workspace_size(const kvq_ctx* ctx, int layer, int batch, int max_context) {
+  int workers = 0;
+  size_t bytes = 0;
+  if (kvq_decode_plan(ctx, layer, batch, max_context, &workers, &bytes) != KVQ_OK) return 0;
+  return bytes;
+}
+
 }  // extern "C"
 
 namespace {

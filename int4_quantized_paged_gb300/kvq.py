@@ -54,6 +54,7 @@ _SIGS = {
     "kvq_cache_write": (i32, [P, i32, P, P, i64, P, i64, P, P, P, P, P, P, P]),
     "kvq_calibrate_per_head": (i32, [P, P, i64, f32, P, P]),
     "kvq_decode_plan": (i32, [P, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(sz)]),
+    "kvq_decode_workspace_size": (sz, [P, i32, i32, i32]),
     "kvq_decode_attention": (i32, [P, i32, P, P, P, P, P, P, P, P, i32, P, i32, i32, P, i32, P,
                                    sz, P]),
     "kvq_prefill_attention": (i32, [P, i32, P, P, P, P, P, P, P, P, i32, P, P, i32, i32, P, P]),
@@ -189,6 +190,10 @@ def kvq_decode_plan(ctx: Context, layer: int, batch: int, max_context: int, num_
     _check(_lib.kvq_decode_plan(ctx, layer, batch, max_context, ctypes.byref(s), ctypes.byref(w)),
            "kvq_decode_plan")
     return s.value, w.value
+
+
+def kvq_decode_workspace_size(ctx: Context, layer: int, batch: int, max_context: int) -> int:
+    return int(_lib.kvq_decode_workspace_size(ctx, layer, batch, max_context))
 
 
 def kvq_decode_attention(ctx: Context, layer: int, q, k_cache, v_cache, block_table,

@@ -155,6 +155,15 @@ def test_decode_plan_and_workspace_rules():
                                   0, ok, 1, None, 0, None) == 0
 
 
+def test_workspace_size_is_the_automatic_plan():
+    ctx = _ctx([3, 0], windows=[0, 128], Hq=64, Hkv=8, D=128)
+    for layer, batch, ctxlen in ((0, 8, 131072), (0, 1, 64), (1, 16, 32768), (0, 0, 0)):
+        assert kvq.kvq_decode_workspace_size(ctx, layer, batch, ctxlen) == \
+            kvq.kvq_decode_plan(ctx, layer, batch, ctxlen)[1]
+    assert kvq.kvq_decode_workspace_size(ctx, 2, 8, 4096) == 0      # no such layer
+    assert kvq.kvq_decode_workspace_size(ctx, 0, -1, 4096) == 0     # invalid batch
+
+
 def test_bf16_output_decode_validates_like_fp32():
     ctx = _ctx([3], Hq=64, Hkv=8, D=128)
     _, ws5 = kvq.kvq_decode_plan(ctx, 0, 8, 131072, num_workers=5)
