@@ -244,7 +244,8 @@ def kvq_decode_attention_fp8_query(ctx: Context, layer: int, q, q_scale, k_cache
     if workspace_bytes is None:
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.kvq_decode_attention_fp8_query(
-        ctx, layer, _ptr(q), _ptr(q_scale), q_scale.numel(), _ptr(k_cache), _ptr(v_cache),
+        ctx, layer, _ptr(q), _ptr(q_scale), 0 if q_scale is None else q_scale.numel(),
+        _ptr(k_cache), _ptr(v_cache),
         _ptr(k_scale), _ptr(v_scale), _ptr(k_cache_scale), _ptr(v_cache_scale),
         _ptr(block_table), mb, _ptr(context_lens), B, max_context, _ptr(out), num_workers,
         _ptr(workspace), workspace_bytes, _stream(stream)), "kvq_decode_attention_fp8_query")

@@ -220,3 +220,12 @@ int main(void) {
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_fp8_query_without_scale_is_an_argument_error():
+    ctx = _ctx([3], Hq=64, Hkv=8, D=128)
+    ok = 0x10000000
+    with pytest.raises(kvq.KVQError, match="INVALID_ARG"):
+        kvq.kvq_decode_attention_fp8_query(ctx, 0, ok, None, ok, ok, ok, ok, ok, max_context=4096,
+                                           k_cache_scale=ok, v_cache_scale=ok, batch=8,
+                                           max_blocks_per_seq=256, stream=0)
