@@ -530,7 +530,8 @@ def run_gpu(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
         "layers": layer_breakdown(layers, dbytes, dec_ms, write_ms),
-        "gpu_launches": 3 * nl * n,
+        # per layer: the write, the decode and (with more than one worker) the merge
+        "gpu_launches": n * sum(3 if lay["workers"] > 1 else 2 for lay in layers),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
