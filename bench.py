@@ -227,13 +227,31 @@ WORKLOADS = {
 }
 
 
-def rank_workload(name: str, rank: int):
+def rank_workload(name: str, rank: int, args=None):
     """The workload a rank runs: the same shapes, its own seed (the path
-    shards by sequence, so each replica draws its own batch)."""
+    shards by sequence, so each replica draws its own batch).  --batch,
+    --context and --layer shrink it (small cases for profiler captures)."""
     import dataclasses
     from int4_quantized_paged_gb300 import workloads as wl
     base = wl.CONFIGS[name]
-    return dataclasses.replace(base, seed=base.seed + 1000 * rank)
+    w = dataclasses.replace(base, seed=base.seed + 1000 * rank)
+    if args is not None and (getattr(args, "batch", 0) or getattr(args, "context", 0)):
+        w = wl.scaled(w, batch=args.batch or None, context=args.context or None)
+    if args is not None and getattr(args, "layer", None) is not None:
+        w = dataclasses.replace(w, windows=(w.windows[args.layer],))
+    return w
+
+
+def shape_note(args) -> str:
+    """Text appended to the workload description when the shape was shrunk."""
+    parts = []
+    if getattr(args, "batch", 0):
+        parts.append(f"batch {args.batch}")
+    if getattr(args, "context", 0):
+        parts.append(f"context {args.context}")
+    if getattr(args, "layer", None) is not None:
+        parts.append(f"layer {args.layer} only")
+    return f" [reduced: {', '.join(parts)}]" if parts else ""
 
 
 def layer_modes(w, mode: int, skip_sliding: bool):
@@ -249,7 +267,7 @@ def setup_gpu(args, dev, rank, w=None, time_fill=True):
     from int4_quantized_paged_gb300 import kvq
     from int4_quantized_paged_gb300 import workloads as wl
 
-    w = rank_workload(args.workload, rank) if w is None else w
+    w = rank_workload(args.workload, rank, args) if w is None else w
     L = w.context_lens[0]
     modes = layer_modes(w, kvq.MODE_NAMES[args.mode], args.skip_sliding)
     pg = wl.paging(w, dev)
@@ -509,7 +527,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": {0: "bf16", 4: "int4"}.get(layers[top]["mode"], "fp8_e4m3"),
         "data": "synthetic (seeded; N(0,1) with the workload's per-head multipliers and outliers)",
-        "config": {"workload": WORKLOADS[args.workload], "mode": mode_name,
+        "config": {"workload": WORKLOADS[args.workload] + shape_note(args), "mode": mode_name,
                    "num_workers": layers[top]["workers"], "cuda_graph": bool(graph is not None),
                    "l2": "inputs larger than L2: %.0f MB of cache read per step vs 129 MB L2"
                          % (sum(dbytes) / 1e6),
@@ -883,6 +901,12 @@ def main(argv=None):
     ap.add_argument("--graph", dest="graph", action="store_true", default=None,
                     help="replay the step as a CUDA graph (default: on for multi-layer steps)")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload at this batch instead of its own (0: its own)")
+    ap.add_argument("--context", type=int, default=0,
+                    help="run the workload at this context instead of its own (0: its own)")
+    ap.add_argument("--layer", type=int, default=None,
+                    help="run only this layer of the workload (its window and mode)")
     ap.add_argument("--cpu-seqs", type=int, default=0, help="0: the workload's default sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--latency-sweep", action="store_true",

@@ -62,5 +62,9 @@ def build(force: bool = False, verbose: bool = False, extra: list | None = None)
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True,
-                extra=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None))
+    # --force rebuilds every object; --ptxas-v prints register and spill
+    # counts; -DNAME=VALUE arguments set the kernels' build-time knobs
+    extra = [a for a in sys.argv[1:] if a.startswith("-D")]
+    if "--ptxas-v" in sys.argv:
+        extra += ["-Xptxas", "-v"]
+    print(build(force="--force" in sys.argv or bool(extra), verbose=True, extra=extra or None))

@@ -71,6 +71,9 @@ constexpr int WARPS = 4;         // worker warps per CTA (independent)
 #ifndef KVQ_QK2
 #define KVQ_QK2 1
 #endif
+#ifndef KVQ_SCORE_FMA
+#define KVQ_SCORE_FMA 0
+#endif
 constexpr int PAIR = KVQ_TILES_PER_ITER;   // 16-position tiles per loop iteration
 constexpr int TILE = 16;         // positions per tile
 constexpr int KP = 13;           // P' = p v_scale 2^(KP - vexp) < 2^14 (dynamic scales)
@@ -787,15 +790,34 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     // ---------------- scores (log2 units); masked entries are -inf
     float s_raw[PAIR][4];
     float vsr[PAIR][2];
+#if KVQ_SCORE_FMA
+    // The score before the column factor as an unevaluated sum hi + lo (the
+    // exact product of the MMA result and the position's K scale), so that
+    // the exponent below is formed with one rounding at the size of
+    // score - max rather than two at the size of the score.
+    float shi[PAIR][4], slo[PAIR][4];
+#endif
     int et_loc = -1000;             // largest V-scale exponent of this lane's retained rows
 #pragma unroll
     for (int u = 0; u < PAIR; ++u) {
       float kf0 = s_fac, kf1 = s_fac;
       vsr[u][0] = vsr[u][1] = 1.f;
+#if KVQ_SCORE_FMA
+#pragma unroll
+      for (int e = 0; e < 4; ++e) { shi[u][e] = sacc[u][e]; slo[u][e] = 0.f; }
+#endif
       if constexpr (C::DYN) {
         if (ok[u]) {
           kf0 = s_fac * ksc[u][lg];
           kf1 = s_fac * ksc[u][lg + 8];
+#if KVQ_SCORE_FMA
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float kr = (e & 2) ? ksc[u][lg + 8] : ksc[u][lg];
+            shi[u][e] = sacc[u][e] * kr;
+            slo[u][e] = fmaf(sacc[u][e], kr, -shi[u][e]);
+          }
+#endif
           vsr[u][0] = ksc[u][16 + lg];
           vsr[u][1] = ksc[u][16 + lg + 8];
           // rows outside [lo, L) may hold anything: only retained rows count
@@ -869,11 +891,23 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     for (int c = 0; c < 2; ++c) {
       // m_run is -inf only while every score so far is -inf: weights 0
       const float mu = (m_run[c] == -INFINITY) ? 0.f : m_run[c];
+#if KVQ_SCORE_FMA
+      const float fc = s_fac * qc[c];               // the column's score factor
+#endif
       float sum = 0.f;
 #pragma unroll
       for (int u = 0; u < PAIR; ++u) {
+#if KVQ_SCORE_FMA
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int e = c + 2 * r;
+          const float t = fmaf(slo[u][e], fc, fmaf(shi[u][e], fc, -mu));
+          pw[u][e] = (s_raw[u][e] == -INFINITY) ? 0.f : ex2(t);
+        }
+#else
         pw[u][c] = ex2(s_raw[u][c] - mu);
         pw[u][c + 2] = ex2(s_raw[u][c + 2] - mu);
+#endif
         sum += pw[u][c] + pw[u][c + 2];
       }
       l_run[c] += sum;
