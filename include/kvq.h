@@ -64,9 +64,13 @@ typedef enum kvq_mode {
   KVQ_INT4_PER_TOKEN_HEAD = 4  /* packed symmetric INT4, scale = amax/7 */
 } kvq_mode;
 
-/* Model/cache description, the pages' statement of the problem: layers, Hq,
- * Hkv, head size, block size, per-layer scale mode, window and skipped
- * (KVQ_BF16) layers. */
+/* Model/cache description, the pages' statement of the problem: layers, Hq
+ * query heads and Hkv KV heads ([P3] "Per-head scales have fixed overhead"),
+ * head size and block size ([P2] "Per-token-head KV cache scale overhead",
+ * "Convert bytes into block capacity"), the scale layout of each layer ([P1]
+ * "Per-tensor vs per-head FP8 KV cache scales"), and the window and skipped
+ * (KVQ_BF16) layers ([P3] "FP8 KV cache layer skipping vs per-head scales",
+ * "Layer skipping follows retained-token footprint"). */
 typedef struct kvq_config {
   int num_layers;
   int num_q_heads;          /* Hq; a multiple of num_kv_heads, Hq/Hkv <= 16 */
@@ -82,15 +86,27 @@ typedef struct kvq_config {
 
 typedef struct kvq_ctx kvq_ctx;
 
-/* Validates and copies *cfg.  Host only; no CUDA call. */
+/* Validates and copies *cfg into a new context (the description above;
+ * [P1] and [P3] as cited there).  Host only; no CUDA call.  Returns
+ * KVQ_ERR_INVALID_ARG for a null pointer, a non-positive count, Hq not a
+ * multiple of Hkv, a mode outside kvq_mode or a negative window, and
+ * KVQ_ERR_UNSUPPORTED for a head size, block size or GQA ratio that is not
+ * built or a cache too large for 32-bit cell indices.  *out is NULL on
+ * error; the caller releases a context with kvq_destroy. */
 kvq_status kvq_create(const kvq_config* cfg, kvq_ctx** out);
 void kvq_destroy(kvq_ctx* ctx);
 
 /* Bytes of one layer's K code buffer and K scale buffer (V is the same).
  * Codes: [num_blocks][Hkv][block_size][row] with row = 2D (BF16), D (FP8) or
- * D/2 (INT4) bytes.  Scales (dynamic modes only, else 0): [num_blocks][Hkv]
- * [block_size] fp32.  Each (block, head) page of codes and of scales is
- * contiguous.  Host only. */
+ * D/2 (INT4) bytes ([P2] "The FP8 scale tax is 4 divided by head size": one
+ * byte per FP8 element; "INT4 makes the metadata fraction larger": half a
+ * byte per INT4 element).  Scales (dynamic modes only, else 0): [num_blocks]
+ * [Hkv][block_size] fp32, one K and one V scale per token and KV head
+ * (same section; the pages' padding of each scale is not stored).  Each
+ * (block, head) page of codes and of scales is contiguous; a block of
+ * block_size tokens holds block_size x the per-token bytes ([P2] "Convert
+ * bytes into block capacity").  Host only; KVQ_ERR_INVALID_ARG for a bad
+ * context or layer.  The caller allocates the buffers. */
 kvq_status kvq_layer_buffer_sizes(const kvq_ctx* ctx, int layer, size_t* code_bytes,
                                   size_t* scale_bytes);
 
@@ -150,7 +166,10 @@ kvq_status kvq_calibrate_per_head(const kvq_ctx* ctx, const void* x, long long n
  * head) items are cut into 16-position tiles and divided evenly among
  * `num_workers` worker warps (split-K over the context, balanced whatever the
  * context lengths); an item shared by several workers is merged by
- * log-sum-exp.  On input *num_workers > 0 requests a count, 0 asks for the
+ * log-sum-exp.  The pages fix no decode schedule; split-K with a
+ * log-sum-exp merge is this library's way of spreading the retained
+ * positions of few, long sequences ([P3] "Performance can favor the larger
+ * cache": latency grows with every context token) over every SM.  On input *num_workers > 0 requests a count, 0 asks for the
  * plan's choice (fill every SM, from the batch, KV heads, the longest
  * context and the device); on output it holds the count and
  * *workspace_bytes what a call with that count needs (0 for one worker). */
@@ -165,10 +184,23 @@ size_t kvq_decode_workspace_size(const kvq_ctx* ctx, int layer, int batch, int m
 
 /* Paged decode attention, one query token per sequence.
  *
+ * Scales are folded, never applied element by element: the K scale (per
+ * tensor, per KV head or per token and KV head, [P1] "Per-tensor vs per-head
+ * FP8 KV cache scales", "Range sharing explains the accuracy trade")
+ * multiplies the dot product of q with the raw codes, and the V scale the
+ * softmax weight that meets the raw V codes.  Window layers read only their
+ * last W positions, and KVQ_BF16 layers their native bf16 values ([P3] "FP8
+ * KV cache layer skipping vs per-head scales", "Layer skipping follows
+ * retained-token footprint").  Packed INT4 layers as [P2] "INT4 makes the
+ * metadata fraction larger".
+ *
  * q: bf16 [batch][Hq][D], 16-byte aligned.  Query head hq reads KV head
  *   hq / (Hq/Hkv).
  * block_table: int32 [batch][max_blocks_per_seq]; entries for positions that
- *   are not read may hold anything (e.g. -1).  Only positions [lo, L) are
+ *   are not read may hold anything (e.g. -1).  Row b must cover context_lens[b]
+ *   positions (context_lens[b] <= max_blocks_per_seq x block_size): a longer
+ *   context is an index error -- only the covered positions are read and
+ *   KVQ_ERR_BAD_INDEX is set on the device word.  Only positions [lo, L) are
  *   read, so a window layer may reuse its freed blocks as a ring: with
  *   R = ceil(W / block_size) + 1 physical blocks per sequence, logical block j
  *   may map to ring slot j mod R (the block a new position overwrites holds
@@ -178,7 +210,8 @@ size_t kvq_decode_workspace_size(const kvq_ctx* ctx, int layer, int batch, int m
  *   for a window W, else 0.  L = 0 gives a zero output row.
  * out: fp32 [batch][Hq][D] = sum_p softmax(softmax_scale <q, K_hat[p]>) V_hat[p]
  *   with K_hat = code x K scale, V_hat = code x V scale.
- * max_context: an upper bound of context_lens, used only by the plan.
+ * max_context: an upper bound of context_lens, used only by the plan; more
+ *   than max_blocks_per_seq x block_size returns KVQ_ERR_INVALID_ARG.
  * num_workers: worker warps (see kvq_decode_plan); 0 = the plan's choice.
  *   With more than one worker, partials go to `workspace` (16-byte aligned,
  *   kvq_decode_plan gives its size); its contents need no initialisation.
@@ -249,8 +282,9 @@ kvq_status kvq_decode_attention_bf16(const kvq_ctx* ctx, int layer, const void* 
  * max_query_len: an upper bound of every n_b (sizes the grid; rows past n_b
  *   do no work).
  * Scale pointers and block table as for kvq_decode_attention.  No workspace;
- * n_b > L_b sets the BAD_INDEX bit of the device error word and skips that
- * sequence. */
+ * n_b > L_b, or L_b beyond the positions the sequence's block-table row
+ * covers (max_blocks_per_seq x block_size), sets the BAD_INDEX bit of the
+ * device error word and skips that sequence. */
 kvq_status kvq_prefill_attention(const kvq_ctx* ctx, int layer, const void* q,
                                  const void* k_cache, const void* v_cache, const float* k_scale,
                                  const float* v_scale, const float* k_cache_scale,
@@ -298,6 +332,18 @@ kvq_status kvq_e4m3_encode(const float* in, unsigned char* out, long long n, voi
 /* Synchronizes `stream`, returns the device error word of the current device
  * as a status (KVQ_OK, KVQ_ERR_BAD_INDEX or KVQ_ERR_TIMEOUT) and clears it. */
 kvq_status kvq_get_device_error(void* stream);
+
+/* Check of the timeout path (no counterpart on the pages).  Every wait of the
+ * decode, prefill and staged cache-write kernels on a shared-memory barrier
+ * is bounded (about 2 s); a wait that runs out sets the TIMEOUT bit of the
+ * device error word and the kernel stops instead of hanging the GPU.  This
+ * call enqueues one warp that waits in the same way on a barrier that expects
+ * bytes no copy ever delivers (no copy is issued, so nothing is in flight
+ * when it gives up), with a limit of `limit_cycles` SM clock cycles
+ * (0 < limit_cycles <= 2^31; 2,000,000 is about 1 ms).  Afterwards
+ * kvq_get_device_error() returns KVQ_ERR_TIMEOUT and the context stays
+ * usable.  Returns KVQ_ERR_INVALID_ARG for a limit outside the range. */
+kvq_status kvq_check_bounded_wait(long long limit_cycles, void* stream);
 
 const char* kvq_status_string(kvq_status s);
 

@@ -276,6 +276,9 @@ kvq_status decode_impl(const kvq_ctx* ctx, int layer, const void* q, const float
     return KVQ_ERR_INVALID_ARG;
   if (batch == 0) return KVQ_OK;
   const kvq_config& c = ctx->cfg;
+  // the block-table rows must cover the longest context
+  if ((long long)max_context > (long long)max_blocks_per_seq * c.block_size)
+    return KVQ_ERR_INVALID_ARG;
   const int mode = ctx->mode[layer];
   void* out_any = out ? static_cast<void*>(out) : static_cast<void*>(out_bf16);
   if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out_any)
@@ -454,6 +457,11 @@ kvq_status kvq_prefill_attention(const kvq_ctx* ctx, int layer, const void* q,
 kvq_status kvq_e4m3_encode(const float* in, unsigned char* out, long long n, void* stream) {
   if (n < 0 || (n > 0 && (!in || !out))) return KVQ_ERR_INVALID_ARG;
   return cuda_status(kvq::launch_e4m3_encode(in, out, n, static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_check_bounded_wait(long long limit_cycles, void* stream) {
+  if (limit_cycles <= 0 || limit_cycles > (1LL << 31)) return KVQ_ERR_INVALID_ARG;
+  return cuda_status(kvq::launch_wait_check(limit_cycles, static_cast<cudaStream_t>(stream)));
 }
 
 kvq_status kvq_get_device_error(void* stream) {

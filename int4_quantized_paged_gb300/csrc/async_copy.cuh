@@ -44,12 +44,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait; returns false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait; returns false when `limit` SM clock cycles ran out (the
+// kernels use SPIN_LIMIT_CYCLES; a shorter limit only serves the wait check).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          long long limit = SPIN_LIMIT_CYCLES) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > SPIN_LIMIT_CYCLES) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }

@@ -229,12 +229,18 @@ __device__ __forceinline__ void pv_tile(float (*acc)[D / 16][4], const uint8_t* 
     vc = pos0 + tc >= lo && pos0 + tc < L;
     vd = pos0 + td >= lo && pos0 + td < L;
   }
+  // With 64-byte rows two positions share a 128-byte swizzle row, and if
+  // every lane read its even position first, half of the banks would serve
+  // each load twice.  Lanes with bit 1 of lg set read the odd position of
+  // each pair first (wa <-> wb, wc <-> wd) and select its bytes back with a
+  // swapped byte permutation, so each load touches all 32 banks once.
+  const bool sw = (RB == 64) && ((lg >> 1) & 1);
   uint32_t wa[SW], wb[SW], wc[SW], wd[SW];
   const int seg0 = lg * SEG;
-  load_seg<SEG>(wa, vt, ta * RB + seg0, va);
-  load_seg<SEG>(wb, vt, tb * RB + seg0, vb);
-  load_seg<SEG>(wc, vt, tc * RB + seg0, vc);
-  load_seg<SEG>(wd, vt, td * RB + seg0, vd);
+  load_seg<SEG>(wa, vt, (sw ? tb : ta) * RB + seg0, sw ? vb : va);
+  load_seg<SEG>(wb, vt, (sw ? ta : tb) * RB + seg0, sw ? va : vb);
+  load_seg<SEG>(wc, vt, (sw ? td : tc) * RB + seg0, sw ? vd : vc);
+  load_seg<SEG>(wd, vt, (sw ? tc : td) * RB + seg0, sw ? vc : vd);
 #pragma unroll
   for (int i = 0; i < D / 16; ++i) {
     uint32_t af[4];
@@ -249,7 +255,8 @@ __device__ __forceinline__ void pv_tile(float (*acc)[D / 16][4], const uint8_t* 
       // high nibbles (rows lg + 8: odd d) are read 16x and scaled back in
       // the epilogue
       const int wi = i >> 2, k = i & 3;
-      const uint32_t sel = (uint32_t)(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
+      const uint32_t sel = sw ? (uint32_t)((4 + k) | ((4 + k) << 4) | (k << 8) | (k << 12))
+                              : (uint32_t)(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
       const uint32_t x = __byte_perm(wa[wi], wb[wi], sel);
       const uint32_t y = __byte_perm(wc[wi], wd[wi], sel);
       af[0] = nib2_f16x2<0>(x);
@@ -259,7 +266,7 @@ __device__ __forceinline__ void pv_tile(float (*acc)[D / 16][4], const uint8_t* 
     } else {
       // bytes 2i, 2i+1 of each position's segment
       const int wi = i >> 1;
-      const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+      const uint32_t sel = (i & 1) ? (sw ? 0x3726u : 0x7362u) : (sw ? 0x1504u : 0x5140u);
       e4m3x4_f16(__byte_perm(wa[wi], wb[wi], sel), af[0], af[1]);
       e4m3x4_f16(__byte_perm(wc[wi], wd[wi], sel), af[2], af[3]);
     }
@@ -326,9 +333,23 @@ struct Cursor {
   int n, t0;        // tiles of the item, first tile index (position / 16)
 };
 
+// Positions of sequence b that are read: its context length, at least 0 and
+// at most the positions its block-table row covers (a longer context is an
+// index error: check_len flags it, and only the covered positions are read).
+__device__ __forceinline__ int ctx_len(const DecodeArgs& a, int b) {
+  const int L = a.context_lens[b];
+  const long long cap = (long long)a.max_blocks << a.bs_shift;
+  return L < 0 ? 0 : ((long long)L > cap ? (int)cap : L);
+}
+
+__device__ __forceinline__ void check_len(const DecodeArgs& a, int b) {
+  const int L = a.context_lens[b];
+  if (L < 0 || (long long)L > ((long long)a.max_blocks << a.bs_shift))
+    atomicOr(a.err, ERR_BAD_INDEX);
+}
+
 __device__ __forceinline__ int seq_tiles(const DecodeArgs& a, int b, int* t0) {
-  int L = a.context_lens[b];
-  if (L < 0) L = 0;
+  const int L = ctx_len(a, b);
   const int lo = (a.window > 0 && L > a.window) ? L - a.window : 0;
   *t0 = lo / TILE;
   return L > 0 ? (L + TILE - 1) / TILE - lo / TILE : 0;
@@ -343,7 +364,7 @@ __device__ long long scan_tiles(const DecodeArgs& a, long long find, Cursor* cur
     const int b = b0 + lane;
     int t0 = 0, n = 0;
     if (b < a.B) {
-      if (a.context_lens[b] < 0) atomicOr(a.err, ERR_BAD_INDEX);
+      check_len(a, b);
       n = seq_tiles(a, b, &t0);
     }
     long long incl = (long long)n * a.Hkv;       // inclusive prefix within the chunk
@@ -392,7 +413,7 @@ __device__ int locate(const DecodeArgs& a, int wid, Cursor* cur, int lane) {
     const int b = 32 * i + lane;
     n[i] = t0[i] = 0;
     if (b < a.B) {
-      if (a.context_lens[b] < 0) atomicOr(a.err, ERR_BAD_INDEX);
+      check_len(a, b);
       n[i] = seq_tiles(a, b, &t0[i]);
     }
   }
@@ -688,7 +709,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
       seg_g = cc.g;
       seg_k0 = cc.k;
       seg_n = cc.n;
-      L = a.context_lens[seg_b];
+      L = ctx_len(a, seg_b);
       lo = (a.window > 0 && L > a.window) ? L - a.window : 0;
       __syncwarp();
       // q of this item -> staging -> power-of-two prescale -> f16 B fragments
@@ -790,19 +811,21 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     // ---------------- scores (log2 units); masked entries are -inf
     float s_raw[PAIR][4];
     float vsr[PAIR][2];
-#if KVQ_SCORE_FMA
+#if KVQ_SCORE_FMA == 1
     // The score before the column factor as an unevaluated sum hi + lo (the
     // exact product of the MMA result and the position's K scale), so that
     // the exponent below is formed with one rounding at the size of
     // score - max rather than two at the size of the score.
     float shi[PAIR][4], slo[PAIR][4];
+#elif KVQ_SCORE_FMA == 2
+    float kqe[PAIR][4];             // score factor of each accumulator element
 #endif
     int et_loc = -1000;             // largest V-scale exponent of this lane's retained rows
 #pragma unroll
     for (int u = 0; u < PAIR; ++u) {
       float kf0 = s_fac, kf1 = s_fac;
       vsr[u][0] = vsr[u][1] = 1.f;
-#if KVQ_SCORE_FMA
+#if KVQ_SCORE_FMA == 1
 #pragma unroll
       for (int e = 0; e < 4; ++e) { shi[u][e] = sacc[u][e]; slo[u][e] = 0.f; }
 #endif
@@ -810,7 +833,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
         if (ok[u]) {
           kf0 = s_fac * ksc[u][lg];
           kf1 = s_fac * ksc[u][lg + 8];
-#if KVQ_SCORE_FMA
+#if KVQ_SCORE_FMA == 1
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float kr = (e & 2) ? ksc[u][lg + 8] : ksc[u][lg];
@@ -834,6 +857,9 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
         const int pos = pos0 + u * TILE + lg + ((e & 2) ? 8 : 0);
         const bool v = ok[u] && (whole || (pos >= lo && pos < L)) && (2 * lt + (e & 1)) < NCOL;
         s_raw[u][e] = v ? sacc[u][e] * kq[e] : -INFINITY;
+#if KVQ_SCORE_FMA == 2
+        kqe[u][e] = kq[e];
+#endif
       }
     }
 
@@ -891,18 +917,28 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     for (int c = 0; c < 2; ++c) {
       // m_run is -inf only while every score so far is -inf: weights 0
       const float mu = (m_run[c] == -INFINITY) ? 0.f : m_run[c];
-#if KVQ_SCORE_FMA
+#if KVQ_SCORE_FMA == 1
       const float fc = s_fac * qc[c];               // the column's score factor
 #endif
       float sum = 0.f;
 #pragma unroll
       for (int u = 0; u < PAIR; ++u) {
-#if KVQ_SCORE_FMA
+#if KVQ_SCORE_FMA == 1
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int e = c + 2 * r;
           const float t = fmaf(slo[u][e], fc, fmaf(shi[u][e], fc, -mu));
           pw[u][e] = (s_raw[u][e] == -INFINITY) ? 0.f : ex2(t);
+        }
+#elif KVQ_SCORE_FMA == 2
+        // score - max in one rounding; in a tile with masked positions their
+        // (arbitrary) products are replaced by -inf
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int e = c + 2 * r;
+          float t = fmaf(sacc[u][e], kqe[u][e], -mu);
+          if (!whole) t = (s_raw[u][e] == -INFINITY) ? -INFINITY : t;
+          pw[u][e] = ex2(t);
         }
 #else
         pw[u][c] = ex2(s_raw[u][c] - mu);

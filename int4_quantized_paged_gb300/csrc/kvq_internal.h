@@ -62,6 +62,8 @@ cudaError_t launch_cache_write(int mode, int D, const WriteArgs& a, cudaStream_t
 cudaError_t launch_calibrate(const uint16_t* x, long long T, int Hkv, int D, float qmax,
                              float* out, cudaStream_t st);
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, long long n, cudaStream_t st);
+// One warp whose bounded barrier wait runs out after limit_cycles (sets TIMEOUT).
+cudaError_t launch_wait_check(long long limit_cycles, cudaStream_t st);
 // Returns cudaErrorInvalidValue for an unsupported (mode, D, G) combination.
 cudaError_t launch_decode(int mode, int D, int G, const DecodeArgs& a, cudaStream_t st);
 bool decode_supported(int mode, int D, int G);

@@ -123,7 +123,9 @@ __global__ void __launch_bounds__(PWARPS * 32, 1)
   const int n_b = pa.query_start[b + 1] - q0;
   int L = a.context_lens[b];
   if (qt * QP >= n_b || n_b <= 0) return;                   // whole CTA: before any barrier
-  if (L < n_b) {                                            // the chunk cannot start before 0
+  // the chunk cannot start before 0, and its last position must lie inside
+  // the positions the sequence's block-table row covers
+  if (L < n_b || (long long)L > ((long long)a.max_blocks << a.bs_shift)) {
     if (tid == 0) atomicOr(a.err, ERR_BAD_INDEX);
     return;
   }

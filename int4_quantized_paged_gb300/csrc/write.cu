@@ -485,6 +485,21 @@ __global__ void calib_finish(unsigned* amax_bits, int Hkv, float qmax) {
   }
 }
 
+// The bounded wait of the decode and cache-write kernels, made to run out:
+// the barrier expects bytes that no copy delivers (none is issued, so nothing
+// is in flight when the wait gives up), and the warp flags TIMEOUT exactly as
+// those kernels do.
+__global__ void wait_check_kernel(unsigned* err, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) mbar_init(&bar, 1);
+  mbar_init_fence();
+  __syncwarp();
+  if (lane == 0) mbar_expect_tx(&bar, 16);
+  __syncwarp();
+  if (!mbar_wait(&bar, 0, limit) && lane == 0) atomicOr(err, ERR_TIMEOUT);
+}
+
 __global__ void e4m3_encode_kernel(const float* in, uint8_t* out, long long n) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
@@ -517,6 +532,13 @@ cudaError_t launch_calibrate(const uint16_t* x, long long T, int Hkv, int D, flo
     calib_amax<<<dim3((unsigned)blocks, (unsigned)Hkv), tb, 0, st>>>(x, T, Hkv, D, bits);
   }
   calib_finish<<<(Hkv + tb - 1) / tb, tb, 0, st>>>(bits, Hkv, qmax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_check(long long limit_cycles, cudaStream_t st) {
+  unsigned* err = error_word();
+  if (!err) return cudaErrorInvalidValue;
+  wait_check_kernel<<<1, 32, 0, st>>>(err, limit_cycles);
   return cudaGetLastError();
 }
 

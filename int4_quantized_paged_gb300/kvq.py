@@ -66,6 +66,7 @@ _SIGS = {
                                                  i32, P, i32, P]),
     "kvq_e4m3_encode": (i32, [P, P, i64, P]),
     "kvq_get_device_error": (i32, [P]),
+    "kvq_check_bounded_wait": (i32, [i64, P]),
     "kvq_status_string": (ctypes.c_char_p, [i32]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -295,6 +296,13 @@ def kvq_e4m3_encode(x, out, n: Optional[int] = None, stream=None):
 def kvq_get_device_error(stream=None) -> int:
     """Synchronizes the stream; returns (and clears) the device error status."""
     return int(_lib.kvq_get_device_error(_stream(stream)))
+
+
+def kvq_check_bounded_wait(limit_cycles: int, stream=None):
+    """Enqueues one warp whose bounded barrier wait runs out after
+    limit_cycles SM cycles and sets the TIMEOUT bit (see include/kvq.h)."""
+    _check(_lib.kvq_check_bounded_wait(int(limit_cycles), _stream(stream)),
+           "kvq_check_bounded_wait")
 
 
 def kvq_status_string(status: int) -> str:

@@ -222,3 +222,38 @@ def test_per_tensor_scale_other_than_one(scale):
     r.write()
     r.check_write()
     r.check_decode(r.decode(num_workers=0), where=f"per-tensor scale {scale}")
+
+
+@pytest.mark.parametrize("workers", [1, 0])
+def test_context_past_its_block_table_row_is_clamped_and_reported(workers):
+    """A context length beyond the positions its block-table row covers is an
+    index error: only the covered positions are read, the BAD_INDEX bit is
+    set, and the other sequences are unaffected.  The table is the front of a
+    larger buffer, so even a read past its last row would stay in allocated
+    memory."""
+    kvq = K()
+    w = SMALL["llama8b"]
+    r = LayerRun(w, orc.FP8_PER_TOKEN_HEAD)
+    r.write()
+    maxb = r.pg.max_blocks
+    cap = maxb * w.block_size
+    padded = torch.zeros(w.B * maxb + 64, dtype=torch.int32, device="cuda")
+    padded[:w.B * maxb] = r.pg.block_table.reshape(-1)
+    bt = padded[:w.B * maxb].view(w.B, maxb)
+    cl = r.pg.context_lens.clone()
+    cl[w.B - 1] = cap + 40
+    q = wl.queries(w, "cuda")
+    nw, ws_bytes = kvq.kvq_decode_plan(r.ctx, 0, w.B, cap, workers)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    out = torch.full((w.B, w.Hq, w.D), float("nan"), device="cuda")
+    with pytest.raises(kvq.KVQError, match="INVALID_ARG"):      # the plan's bound is checked
+        kvq.kvq_decode_attention(r.ctx, 0, q, r.kc, r.vc, bt, cl, out, max_context=cap + 1,
+                                 k_cache_scale=r.ks, v_cache_scale=r.vs, num_workers=nw,
+                                 workspace=ws)
+    kvq.kvq_decode_attention(r.ctx, 0, q, r.kc, r.vc, bt, cl, out, max_context=cap,
+                             k_cache_scale=r.ks, v_cache_scale=r.vs, num_workers=nw, workspace=ws)
+    torch.cuda.synchronize()
+    assert kvq.STATUS[kvq.kvq_get_device_error()] == "KVQ_ERR_BAD_INDEX"
+    assert torch.isfinite(out).all()
+    r.q, r.cl = q, cl.clamp(max=cap)
+    r.check_decode(out, where=f"context past its table row, workers {nw}")
