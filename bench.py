@@ -1,17 +1,20 @@
 """Benchmark of the quantized paged KV cache hot path on one GB300.
 
-One step = one decode step of the Llama-3-8B-like layer (Hq=32, Hkv=8, D=128,
-block 16, batch 64 x context 4096, dynamic per-token-head FP8 by default):
-kvq_cache_write of the current token of every sequence, then
-kvq_decode_attention over the 4096 cached positions.  Throughput is
-algorithmic bytes (what the method must move: codes, scales, q, out, block
-table, new K/V and slots) per second.  The same run also times a
-prefill-shaped cache write of the whole 262,144-token context (cache-write
-GB/s).
+One step = one decode step of the 70B-like long-context layer (Hq=64, Hkv=8,
+D=128, block 16, batch 8 x context 131072, dynamic per-token-head FP8 by
+default): kvq_cache_write of the current token of every sequence, then
+kvq_decode_attention (split-K over the 131,072 cached positions, log-sum-exp
+merge).  Throughput is algorithmic bytes (what the method must move: codes,
+scales, q, out, block table, new K/V and slots) per second.  The same run
+also times a prefill-shaped cache write of the whole 1,048,576-token context
+(cache-write GB/s), and then measures every other workload and mode the same
+way (the "configs" block: decode and fill GB/s and their fractions of the
+measured HBM peak, per-kernel CUDA-event times).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--mode fp8_per_token_head]
-                    [--workload llama8b|llama70b_128k|gptoss20b|gemma_d256]
-                    [--skip-sliding] [--workers N] [--graph | --no-graph]
+                    [--workload llama70b_128k|llama8b|gptoss20b|gemma_d256]
+                    [--skip-sliding] [--workers N] [--graph | --no-graph] [--no-configs]
+                    [--batch B] [--context L] [--layer I]     # smaller cases (profiling)
     python bench.py --impl reference     # the CPU oracle on a bounded sample
     python bench.py --prefill --workload llama8b|gemma_d256     # prefill TFLOP/s
     python bench.py --latency-sweep --workload gptoss20b        # latency vs context
@@ -552,11 +555,121 @@ def run_gpu(args):
         "gpu_launches": n * sum(3 if lay["workers"] > 1 else 2 for lay in layers),
         "clocks": clocks,
     }
+    del st, layers, d_in, d_out, dv, ov
+    if graph is not None:
+        del graph
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_configs:
+        res["configs"] = config_block(args, dev)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args, kvq.MODE_NAMES[args.mode])
     if dist is not None:
         dist.destroy_process_group()
     return res if rank == 0 else None
+
+
+# Every configuration of the five workloads that has a roofline target, each
+# measured in the same run as the headline: (workload, mode, skip sliding).
+CONFIG_BLOCK = [
+    ("llama8b", "fp8_per_tensor", False),
+    ("llama8b", "fp8_per_head", False),
+    ("llama8b", "fp8_per_token_head", False),
+    ("llama8b", "int4_per_token_head", False),
+    ("llama70b_128k", "fp8_per_tensor", False),
+    ("llama70b_128k", "fp8_per_head", False),
+    ("llama70b_128k", "fp8_per_token_head", False),
+    ("gptoss20b", "fp8_per_token_head", False),
+    ("gptoss20b", "fp8_per_token_head", True),
+    ("gemma_d256", "fp8_per_token_head", False),
+    ("gemma_d256", "int4_per_token_head", False),
+]
+
+
+def measure_config(args, dev, workload: str, mode: str, skip: bool, steps: int = 20) -> dict:
+    """One configuration's decode step, timed kernel by kernel with CUDA events
+    on the launching stream, plus its prefill-shaped fill of one full layer.
+    Decode GB/s is the largest layer's decode (+ merge) launch: its
+    algorithmic bytes / its mean event time; the step is the whole write +
+    decode of every layer (a CUDA graph for multi-layer workloads)."""
+    import types
+    import torch
+    from int4_quantized_paged_gb300 import kvq
+    a = types.SimpleNamespace(**{**vars(args), "workload": workload, "mode": mode,
+                                 "skip_sliding": skip, "batch": 0, "context": 0, "layer": None,
+                                 "workers": 0})
+    st = setup_gpu(a, dev, 0)
+    w, layers = st["w"], st["layers"]
+    nl = len(layers)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for li in range(nl):
+            launch_layer(st, li)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nl)]
+          for _ in range(steps)]
+    for i in range(steps):
+        for li in range(nl):
+            launch_layer(st, li, ev[i][li], stream)
+    torch.cuda.synchronize()
+    write_ms = [statistics.mean(ev[i][li][0].elapsed_time(ev[i][li][1]) for i in range(steps))
+                for li in range(nl)]
+    dec_ms = [statistics.mean(ev[i][li][1].elapsed_time(ev[i][li][2]) for i in range(steps))
+              for li in range(nl)]
+    graph = None
+    if nl > 1:
+        graph = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream()
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            step()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(graph, stream=s2):
+                step()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        graph.replay() if graph is not None else step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_step = t0.elapsed_time(t1) / steps
+    if kvq.kvq_get_device_error() != 0:
+        raise RuntimeError(f"device error word set while measuring {workload} {mode}")
+    peak, _ = peak_hbm()
+    dbytes = [decode_bytes(w, lay["mode"], lay["window"]) for lay in layers]
+    wbytes = [write_bytes(w, lay["mode"], w.B) for lay in layers]
+    top = max(range(nl), key=lambda li: dbytes[li] * 1e6 + li)
+    dec_gbs = dbytes[top] / (dec_ms[top] * 1e-3) / 1e9
+    fill_ms, fill_T, fill_mode = st["fill"]
+    wb_fill = write_bytes(w, fill_mode, fill_T)
+    fill_gbs = wb_fill / (fill_ms * 1e-3) / 1e9
+    kv_pos = sum(sum(min(Lb, lay["window"]) if lay["window"] else Lb for Lb in w.context_lens)
+                 for lay in layers)
+    out = {"workload": workload, "mode": mode + ("+bf16_sliding" if skip else ""),
+           "layers": nl, "num_workers": layers[top]["workers"],
+           "decode": {"bytes_per_launch": dbytes[top], "ms": round(dec_ms[top], 5),
+                      "gbs": round(dec_gbs, 2), "frac_of_peak": round(dec_gbs / peak, 4)},
+           "write_fill": {"bytes": wb_fill, "ms": round(fill_ms, 5), "tokens": fill_T,
+                          "gbs": round(fill_gbs, 2), "frac_of_peak": round(fill_gbs / peak, 4)},
+           "write_step_ms": round(sum(write_ms), 5),
+           "decode_step_ms": round(sum(dec_ms), 5),
+           "step": {"ms": round(ms_step, 5), "cuda_graph": graph is not None,
+                    "gbs": round((sum(dbytes) + sum(wbytes)) / (ms_step * 1e-3) / 1e9, 2),
+                    "kv_tokens_per_s": round(kv_pos / (ms_step * 1e-3), 1)}}
+    del st, graph
+    torch.cuda.empty_cache()
+    return out
+
+
+def config_block(args, dev) -> list:
+    return [measure_config(args, dev, wname, mode, skip) for wname, mode, skip in CONFIG_BLOCK]
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -895,7 +1008,7 @@ def main(argv=None):
                     choices=["bf16", "fp8_per_tensor", "fp8_per_head", "fp8_per_token_head",
                              "int4_per_token_head"])
     ap.add_argument("--workers", type=int, default=0)
-    ap.add_argument("--workload", default="llama8b", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="llama70b_128k", choices=sorted(WORKLOADS))
     ap.add_argument("--skip-sliding", action="store_true",
                     help="keep the window layers' caches in BF16 (layer skipping)")
     ap.add_argument("--graph", dest="graph", action="store_true", default=None,
@@ -909,6 +1022,8 @@ def main(argv=None):
                     help="run only this layer of the workload (its window and mode)")
     ap.add_argument("--cpu-seqs", type=int, default=0, help="0: the workload's default sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the block that measures every workload and mode after the headline")
     ap.add_argument("--latency-sweep", action="store_true",
                     help="latency against context for BF16 / FP8 / FP8 + BF16 window layers / "
                          "INT4 instead of the throughput line")

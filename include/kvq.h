@@ -303,10 +303,12 @@ kvq_status kvq_prefill_attention(const kvq_ctx* ctx, int layer, const void* q,
  * Arguments and results are those of kvq_decode_attention without
  * `workspace`/`workspace_bytes`.  The split-K partials live instead in one
  * static device array of KVQ_FIXED_SCRATCH_BYTES (16 MiB) per GPU, held by
- * every GPU that loads the library until the process exits.  A call whose
- * plan (kvq_decode_plan for the same batch, max_context and num_workers)
- * needs more than that returns KVQ_ERR_WORKSPACE and launches nothing; pass a
- * smaller num_workers to fit.
+ * every GPU that loads the library until the process exits.  With
+ * num_workers = 0 the plan's worker count is cut to the most workers whose
+ * partials fit (at worst one worker, which needs no scratch).  An explicit
+ * num_workers whose plan (kvq_decode_plan for the same batch, max_context
+ * and num_workers) needs more than the array returns KVQ_ERR_WORKSPACE and
+ * launches nothing; pass a smaller num_workers to fit.
  *
  * The first call on a device looks the array's address up on that device
  * (make that device current first; make the first call before any stream

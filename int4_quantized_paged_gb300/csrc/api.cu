@@ -510,12 +510,27 @@ kvq_status kvq_decode_attention_fixed_scratch(const kvq_ctx* ctx, int layer, con
   kvq_status st = check_layer(ctx, layer);
   if (st != KVQ_OK) return st;
   if (batch < 0 || max_context < 0 || num_workers < 0) return KVQ_ERR_INVALID_ARG;
-  // Size check first: a plan whose partials do not fit is refused.
+  // Size check first.  An explicit worker count whose partials do not fit is
+  // refused; the automatic plan is cut to the most workers that fit (one
+  // worker needs no scratch at all).
   int workers = num_workers;
   size_t need = 0;
   st = kvq_decode_plan(ctx, layer, batch, max_context, &workers, &need);
   if (st != KVQ_OK) return st;
-  if (need > (size_t)KVQ_FIXED_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;
+  if (need > (size_t)KVQ_FIXED_SCRATCH_BYTES) {
+    if (num_workers > 0) return KVQ_ERR_WORKSPACE;
+    const kvq_config& c = ctx->cfg;
+    const long long items = (long long)batch * c.num_kv_heads;
+    const long long G = c.num_q_heads / c.num_kv_heads;
+    const long long per_slot = G * (c.head_dim + 2) * (long long)sizeof(float);
+    const long long room = (long long)KVQ_FIXED_SCRATCH_BYTES - (items + 1) * (long long)sizeof(long long);
+    long long fit = room > 0 ? room / per_slot - items : 0;
+    if (fit > workers) fit = workers;
+    workers = fit >= 2 ? (int)fit : 1;
+    st = kvq_decode_plan(ctx, layer, batch, max_context, &workers, &need);
+    if (st != KVQ_OK) return st;
+    if (need > (size_t)KVQ_FIXED_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;
+  }
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
   void* scratch = nullptr;

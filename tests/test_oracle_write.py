@@ -240,3 +240,48 @@ def test_fp8_dynamic_hand_computed_codes():
     assert s == 1.0
     assert list(row[:6]) == [0x7E, 0xF6, 0x38, 0x2A, 0x01, 0xD8]
     assert not row[6:].any()
+
+
+def _static_write(mode, k_scale, v_scale, values, D=64):
+    """One token, two KV heads, both heads' K and V holding `values` (then
+    zeros), written with distinct K and V scales; returns the K and V code
+    rows [2, D]."""
+    x = torch.zeros((1, 2, D), dtype=torch.bfloat16)
+    x[0, :, :len(values)] = torch.tensor(values, dtype=torch.float64).to(torch.bfloat16)
+    xb = bits(x)
+    kc, vc, _, _ = orc.alloc_cache(mode, 1, 2, 16, D)
+    orc.cache_write(mode, xb, xb, np.zeros(1, dtype=np.int64), kc, vc, None, None,
+                    k_scale=np.asarray(k_scale, dtype=np.float32),
+                    v_scale=np.asarray(v_scale, dtype=np.float32))
+    return kc[0, :, 0], vc[0, :, 0]
+
+
+# E4M3 codes worked out by hand (bias 7; code = sign | E << 3 | M, value
+# 2^(E-7) (1 + M/8)) for the quotients y = x / s of x = 1, -3, 100, 300:
+#   y = 2 -> 0x40, -6 -> 0xCC, 200 (halfway 192|208, even M) -> 0x74, 600 -> 0x7E (saturated)
+#   y = 0.25 -> 0x28, -0.75 -> 0xB4, 25 (halfway 24|26) -> 0x5C, 75 (-> 72) -> 0x69
+#   y = 0.5 -> 0x30, -1.5 -> 0xBC, 50 (halfway 48|52) -> 0x64, 150 (-> 144) -> 0x71
+#   y = 4 -> 0x48, -12 -> 0xD4, 400 (halfway 384|416) -> 0x7C, 1200 -> 0x7E
+HAND = {0.5: [0x40, 0xCC, 0x74, 0x7E], 4.0: [0x28, 0xB4, 0x5C, 0x69],
+        2.0: [0x30, 0xBC, 0x64, 0x71], 0.25: [0x48, 0xD4, 0x7C, 0x7E]}
+VALUES = [1, -3, 100, 300]
+
+
+def test_static_per_head_distinct_k_and_v_scales_hand_computed():
+    """Static per-head FP8 ("Per-tensor vs per-head FP8 KV cache scales",
+    section "Static per-head metadata is almost free": one K and one V scale
+    per KV head): head h of K divides by k_scale[h], head h of V by
+    v_scale[h].  Four distinct scales, so a K/V or a head swap changes bytes."""
+    kc, vc = _static_write(orc.FP8_PER_HEAD, [0.5, 4.0], [2.0, 0.25], VALUES)
+    assert list(kc[0, :4]) == HAND[0.5] and list(kc[1, :4]) == HAND[4.0]
+    assert list(vc[0, :4]) == HAND[2.0] and list(vc[1, :4]) == HAND[0.25]
+    assert not kc[:, 4:].any() and not vc[:, 4:].any()
+
+
+def test_per_tensor_distinct_k_and_v_scales_hand_computed():
+    """Per-tensor FP8 (same page and section: one K and one V scale per
+    layer): every head of K divides by k_scale[0], every head of V by
+    v_scale[0]."""
+    kc, vc = _static_write(orc.FP8_PER_TENSOR, [0.5], [2.0], VALUES)
+    assert list(kc[0, :4]) == HAND[0.5] and list(kc[1, :4]) == HAND[0.5]
+    assert list(vc[0, :4]) == HAND[2.0] and list(vc[1, :4]) == HAND[2.0]

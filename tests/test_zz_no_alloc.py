@@ -53,8 +53,8 @@ def test_fixed_scratch_full_size_llama8b():
     r = LayerRun(w, orc.FP8_PER_TOKEN_HEAD)
     r.write()
     ref_out = r.decode(num_workers=0)
-    out = torch.full_like(ref_out, float("nan"))
     for _ in range(2):
+        out = torch.full_like(ref_out, float("nan"))     # each call must write every row
         _fixed(r, out, 0)
         torch.cuda.synchronize()
         pairs = sample_pairs(w, 24, seed=5)
@@ -76,3 +76,25 @@ def test_fixed_scratch_refuses_a_plan_that_does_not_fit():
     with pytest.raises(kvq.KVQError, match="WORKSPACE"):
         _fixed(r, out, workers)
     assert torch.all(out == 0)
+
+
+def test_fixed_scratch_automatic_plan_shrinks_to_fit():
+    """With num_workers = 0 the automatic plan is cut to what the array holds:
+    here 1024 sequences x 8 KV heads at D = 256 need more than 16 MiB for the
+    per-item slots alone, so the call runs on one worker (no scratch) and
+    still matches the workspace entry point."""
+    kvq = K()
+    w = wl.Workload("wide256", Hq=16, Hkv=8, D=256, block_size=16,
+                    context_lens=tuple([40] * 1024), windows=(0,), seed=97)
+    r = LayerRun(w, orc.FP8_PER_TOKEN_HEAD)
+    _, need = kvq.kvq_decode_plan(r.ctx, 0, w.B, 40, 0)
+    r.write()
+    ref_out = r.decode(num_workers=0)
+    assert r.workers > 1 and need > 16 * 1024 * 1024
+    for _ in range(2):
+        out = torch.full_like(ref_out, float("nan"))
+        _fixed(r, out, 0)
+        torch.cuda.synchronize()
+        assert K().kvq_get_device_error() == 0
+        assert torch.allclose(out, ref_out, rtol=1e-5, atol=1e-5)
+    r.check_decode(out, pairs=sample_pairs(w, 32, seed=3), where="fixed scratch shrunk plan")
