@@ -71,9 +71,6 @@ constexpr int WARPS = 4;         // worker warps per CTA (independent)
 #ifndef KVQ_QK2
 #define KVQ_QK2 1
 #endif
-#ifndef KVQ_SCORE_FMA
-#define KVQ_SCORE_FMA 0
-#endif
 constexpr int PAIR = KVQ_TILES_PER_ITER;   // 16-position tiles per loop iteration
 constexpr int TILE = 16;         // positions per tile
 constexpr int KP = 13;           // P' = p v_scale 2^(KP - vexp) < 2^14 (dynamic scales)
@@ -811,36 +808,15 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     // ---------------- scores (log2 units); masked entries are -inf
     float s_raw[PAIR][4];
     float vsr[PAIR][2];
-#if KVQ_SCORE_FMA == 1
-    // The score before the column factor as an unevaluated sum hi + lo (the
-    // exact product of the MMA result and the position's K scale), so that
-    // the exponent below is formed with one rounding at the size of
-    // score - max rather than two at the size of the score.
-    float shi[PAIR][4], slo[PAIR][4];
-#elif KVQ_SCORE_FMA == 2
-    float kqe[PAIR][4];             // score factor of each accumulator element
-#endif
     int et_loc = -1000;             // largest V-scale exponent of this lane's retained rows
 #pragma unroll
     for (int u = 0; u < PAIR; ++u) {
       float kf0 = s_fac, kf1 = s_fac;
       vsr[u][0] = vsr[u][1] = 1.f;
-#if KVQ_SCORE_FMA == 1
-#pragma unroll
-      for (int e = 0; e < 4; ++e) { shi[u][e] = sacc[u][e]; slo[u][e] = 0.f; }
-#endif
       if constexpr (C::DYN) {
         if (ok[u]) {
           kf0 = s_fac * ksc[u][lg];
           kf1 = s_fac * ksc[u][lg + 8];
-#if KVQ_SCORE_FMA == 1
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float kr = (e & 2) ? ksc[u][lg + 8] : ksc[u][lg];
-            shi[u][e] = sacc[u][e] * kr;
-            slo[u][e] = fmaf(sacc[u][e], kr, -shi[u][e]);
-          }
-#endif
           vsr[u][0] = ksc[u][16 + lg];
           vsr[u][1] = ksc[u][16 + lg + 8];
           // rows outside [lo, L) may hold anything: only retained rows count
@@ -857,9 +833,6 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
         const int pos = pos0 + u * TILE + lg + ((e & 2) ? 8 : 0);
         const bool v = ok[u] && (whole || (pos >= lo && pos < L)) && (2 * lt + (e & 1)) < NCOL;
         s_raw[u][e] = v ? sacc[u][e] * kq[e] : -INFINITY;
-#if KVQ_SCORE_FMA == 2
-        kqe[u][e] = kq[e];
-#endif
       }
     }
 
@@ -917,33 +890,11 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     for (int c = 0; c < 2; ++c) {
       // m_run is -inf only while every score so far is -inf: weights 0
       const float mu = (m_run[c] == -INFINITY) ? 0.f : m_run[c];
-#if KVQ_SCORE_FMA == 1
-      const float fc = s_fac * qc[c];               // the column's score factor
-#endif
       float sum = 0.f;
 #pragma unroll
       for (int u = 0; u < PAIR; ++u) {
-#if KVQ_SCORE_FMA == 1
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int e = c + 2 * r;
-          const float t = fmaf(slo[u][e], fc, fmaf(shi[u][e], fc, -mu));
-          pw[u][e] = (s_raw[u][e] == -INFINITY) ? 0.f : ex2(t);
-        }
-#elif KVQ_SCORE_FMA == 2
-        // score - max in one rounding; in a tile with masked positions their
-        // (arbitrary) products are replaced by -inf
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int e = c + 2 * r;
-          float t = fmaf(sacc[u][e], kqe[u][e], -mu);
-          if (!whole) t = (s_raw[u][e] == -INFINITY) ? -INFINITY : t;
-          pw[u][e] = ex2(t);
-        }
-#else
         pw[u][c] = ex2(s_raw[u][c] - mu);
         pw[u][c + 2] = ex2(s_raw[u][c + 2] - mu);
-#endif
         sum += pw[u][c] + pw[u][c + 2];
       }
       l_run[c] += sum;
@@ -968,26 +919,49 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
       if (!ok[u]) continue;
       const float pr[4] = {pw[u][0], pw[u][1], pw[u][2], pw[u][3]};
       uint32_t pb[NT][2];
+      if constexpr (C::BF) {
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        float x[4];
+        for (int n = 0; n < NT; ++n) {
+          float x[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 2 * lt + (e & 1);
-          const int k = PACKED ? c / G : n;
-          const bool live = PACKED ? (k < NPART) : (c < G);
-          x[e] = live ? split_term<C::BF>(pr[e], k) : 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const int c = 2 * lt + (e & 1);
+            const int k = PACKED ? c / G : n;
+            const bool live = PACKED ? (k < NPART) : (c < G);
+            x[e] = live ? split_term<true>(pr[e], k) : 0.f;
+          }
+          pb[n][0] = movmatrix_t(pack_bf16x2(x[0], x[1]));   // positions 0..7
+          pb[n][1] = movmatrix_t(pack_bf16x2(x[2], x[3]));   // positions 8..15
         }
-        uint32_t p0, p1;
-        if constexpr (C::BF) {
-          p0 = pack_bf16x2(x[0], x[1]);
-          p1 = pack_bf16x2(x[2], x[3]);
+      } else {
+        // f16 hi + lo: the hi pairs are packed once, the lo pairs are the
+        // remainders of their unpacked values
+        const uint32_t h01 = pack_f16x2(pr[0], pr[1]), h23 = pack_f16x2(pr[2], pr[3]);
+        const uint32_t l01 = pack_f16x2(pr[0] - f16_lo(h01), pr[1] - f16_hi(h01));
+        const uint32_t l23 = pack_f16x2(pr[2] - f16_lo(h23), pr[3] - f16_hi(h23));
+        if constexpr (PACKED) {
+          // column c carries term c / G of head c % G: lanes whose two
+          // columns are hi columns take the hi pair, the next G columns the
+          // lo pair, dead columns zero (G = 1: column 0 hi, column 1 lo)
+          uint32_t p01, p23;
+          if constexpr (G == 1) {
+            p01 = lt == 0 ? __byte_perm(h01, l01, 0x7610) : 0u;
+            p23 = lt == 0 ? __byte_perm(h23, l23, 0x7610) : 0u;
+          } else {
+            const int k = (2 * lt) / G;
+            p01 = k == 0 ? h01 : (k == 1 ? l01 : 0u);
+            p23 = k == 0 ? h23 : (k == 1 ? l23 : 0u);
+          }
+          pb[0][0] = movmatrix_t(p01);
+          pb[0][1] = movmatrix_t(p23);
         } else {
-          p0 = pack_f16x2(x[0], x[1]);
-          p1 = pack_f16x2(x[2], x[3]);
+          // one column tile per term; columns past G are zero
+          const bool live = 2 * lt < G;
+          pb[0][0] = movmatrix_t(live ? h01 : 0u);
+          pb[0][1] = movmatrix_t(live ? h23 : 0u);
+          pb[NT - 1][0] = movmatrix_t(live ? l01 : 0u);
+          pb[NT - 1][1] = movmatrix_t(live ? l23 : 0u);
         }
-        pb[n][0] = movmatrix_t(p0);       // positions 0..7
-        pb[n][1] = movmatrix_t(p1);       // positions 8..15
       }
       const uint8_t* vt = kt[u] + C::TBP;
       const int pb0 = pos0 + u * TILE;

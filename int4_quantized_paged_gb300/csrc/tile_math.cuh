@@ -11,9 +11,12 @@
 
 namespace kvq {
 
+// 2^x, flushing results below 2^-126 to zero: every use is a softmax weight
+// or a rescale factor relative to a running maximum, where such a value is
+// negligible beside the weight 1 of the maximum itself.
 __device__ __forceinline__ float ex2(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -88,6 +91,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float f16_lo(uint32_t h2) {
   float f;
   asm("{ .reg .b16 a, b; mov.b32 {a, b}, %1; cvt.f32.f16 %0, a; }" : "=f"(f) : "r"(h2));
+  return f;
+}
+__device__ __forceinline__ float f16_hi(uint32_t h2) {
+  float f;
+  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %1; cvt.f32.f16 %0, b; }" : "=f"(f) : "r"(h2));
   return f;
 }
 __device__ __forceinline__ float bf16_lo(uint32_t h2) { return __uint_as_float(h2 << 16); }
