@@ -62,16 +62,11 @@ namespace kvq {
 namespace {
 
 constexpr int WARPS = 4;         // worker warps per CTA (independent)
-// Tuning knobs (build-time): tiles per loop iteration (1 measured best; 2
-// shares the softmax reductions between two tiles at the cost of registers)
-// and the QK accumulator chains (2 shortens the MMA dependency chain).
-#ifndef KVQ_TILES_PER_ITER
-#define KVQ_TILES_PER_ITER 1
-#endif
+// Tuning knob (build-time): the QK accumulator chains (2 shortens the MMA
+// dependency chain).
 #ifndef KVQ_QK2
 #define KVQ_QK2 1
 #endif
-constexpr int PAIR = KVQ_TILES_PER_ITER;   // 16-position tiles per loop iteration
 constexpr int TILE = 16;         // positions per tile
 constexpr int KP = 13;           // P' = p v_scale 2^(KP - vexp) < 2^14 (dynamic scales)
 
@@ -311,10 +306,10 @@ struct Layout {
   // slack).
   static constexpr int budget = 233472 / MinCtas<MODE, D, G>::value - 2048;
   static constexpr int fit(int ns) {
-    return (ns > PAIR + 1 && WARPS * warp_bytes(ns) > budget) ? fit(ns - 1) : ns;
+    return (ns > 2 && WARPS * warp_bytes(ns) > budget) ? fit(ns - 1) : ns;
   }
 #ifdef KVQ_NS
-  static constexpr int NS = KVQ_NS < PAIR + 1 ? PAIR + 1 : KVQ_NS;
+  static constexpr int NS = KVQ_NS < 2 ? 2 : KVQ_NS;
 #else
   static constexpr int NS = fit((D == 256 && MODE != BF16) ? 3 : 2);
 #endif
@@ -609,7 +604,9 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
   float acc[NT][C::MTILES][4];
   int vexp = -1000;               // running max exponent of the V scales (dynamic)
   float fv = 0.f;                 // 2^(KP - vexp)
+  float vcap = 0.f;               // 2^(vexp + 1): a V scale at or above it raises vexp
   float qc[2] = {1.f, 1.f};       // per-column query scale (FP8 query, per-head scales)
+  float sq[2] = {0.f, 0.f};       // score factor of each column: s_fac x qc
   int seg_b = -1, seg_g = -1, seg_k0 = 0, seg_klast = 0, seg_n = 0;
 
   // Writes the segment's result: final output if it covered the whole item,
@@ -762,10 +759,13 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
           qf[s][1] = pack_f16x2(v[2], v[3]);
         }
       }
+      sq[0] = s_fac * qc[0];
+      sq[1] = s_fac * qc[1];
       m_run[0] = m_run[1] = -INFINITY;
       l_run[0] = l_run[1] = 0.f;
       vexp = -1000;
       fv = 0.f;
+      vcap = 0.f;
 #pragma unroll
       for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -774,65 +774,51 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
           for (int e = 0; e < 4; ++e) acc[n][i][e] = 0.f;
     }
 
-    // ---------------- this iteration: tiles j and j+1 when both are in the item
-    const int cnt = (PAIR == 2 && j + 1 < ntiles && cc.k + 1 < cc.n) ? 2 : 1;
+    // ---------------- this iteration: tile j
     const int pos0 = (cc.t0 + cc.k) * TILE;
-    bool ok[PAIR];
-    const uint8_t* kt[PAIR];
-    const float* ksc[PAIR];
-#pragma unroll
-    for (int u = 0; u < PAIR; ++u) {
-      const int st = (cst + u < NS) ? cst + u : cst + u - NS;
-      const uint32_t par = (cst + u < NS) ? cpar : cpar ^ 1u;
-      ok[u] = u < cnt && ((valid_mask >> st) & 1u);
-      kt[u] = wcodes + st * C::STAGE;
-      ksc[u] = wscales + st * 32;
-      if (ok[u] && !mbar_wait(&wbars[st], par)) fail_at = j;
+    const bool ok = (valid_mask >> cst) & 1u;
+    const uint8_t* kt = wcodes + cst * C::STAGE;
+    const float* ksc = wscales + cst * 32;
+    if (ok && !mbar_wait(&wbars[cst], cpar)) {
+      fail_at = j;
+      break;
     }
-    if (fail_at >= 0) break;
-    // whole: every position of the (up to) 32 is retained, so nothing is masked
-    bool all_ok = true;
-#pragma unroll
-    for (int u = 0; u < PAIR; ++u) all_ok = all_ok && (u >= cnt || ok[u]);
-    const bool whole = all_ok && pos0 >= lo && pos0 + cnt * TILE <= L;
+    // whole: every position of the tile is retained, so nothing is masked
+    const bool whole = ok && pos0 >= lo && pos0 + TILE <= L;
 
-    // ---------------- QK: rows lg, lg+8 of each sub-tile
-    float sacc[PAIR][4];
-#pragma unroll
-    for (int u = 0; u < PAIR; ++u) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sacc[u][e] = 0.f;
-      if (ok[u]) qk_tile<MODE, D>(sacc[u], kt[u], lg, lt, qf);
-    }
+    // ---------------- QK: rows lg, lg+8
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok) qk_tile<MODE, D>(sacc, kt, lg, lt, qf);
 
     // ---------------- scores (log2 units); masked entries are -inf
-    float s_raw[PAIR][4];
-    float vsr[PAIR][2];
-    int et_loc = -1000;             // largest V-scale exponent of this lane's retained rows
-#pragma unroll
-    for (int u = 0; u < PAIR; ++u) {
-      float kf0 = s_fac, kf1 = s_fac;
-      vsr[u][0] = vsr[u][1] = 1.f;
-      if constexpr (C::DYN) {
-        if (ok[u]) {
-          kf0 = s_fac * ksc[u][lg];
-          kf1 = s_fac * ksc[u][lg + 8];
-          vsr[u][0] = ksc[u][16 + lg];
-          vsr[u][1] = ksc[u][16 + lg + 8];
-          // rows outside [lo, L) may hold anything: only retained rows count
-          const int p0 = pos0 + u * TILE + lg, p1 = p0 + 8;
-          if (whole || (p0 >= lo && p0 < L)) et_loc = max(et_loc, f32_exp(vsr[u][0]));
-          if (whole || (p1 >= lo && p1 < L)) et_loc = max(et_loc, f32_exp(vsr[u][1]));
-        }
+    // score factor of each accumulator element: the row's K scale (dynamic)
+    // times the column factor, formed apart from the QK result so it stays
+    // off its dependency chain
+    float kq[4] = {sq[0], sq[1], sq[0], sq[1]};
+    float vs0 = 1.f, vs1 = 1.f;           // V scales of rows lg, lg + 8 (dynamic)
+    bool vraise = false;                  // a retained row's V scale reaches 2^(vexp + 1)
+    if constexpr (C::DYN) {
+      if (ok) {
+        const float k0 = ksc[lg], k1 = ksc[lg + 8];
+        kq[0] = k0 * sq[0]; kq[1] = k0 * sq[1]; kq[2] = k1 * sq[0]; kq[3] = k1 * sq[1];
+        vs0 = ksc[16 + lg];
+        vs1 = ksc[16 + lg + 8];
+        // rows outside [lo, L) may hold anything: only retained rows count
+        const int p0 = pos0 + lg, p1 = p0 + 8;
+        vraise = ((whole || (p0 >= lo && p0 < L)) && vs0 >= vcap) ||
+                 ((whole || (p1 >= lo && p1 < L)) && vs1 >= vcap);
       }
-      // score factors per accumulator element (row scale times column scale),
-      // formed apart from the QK result so they stay off its dependency chain
-      const float kq[4] = {kf0 * qc[0], kf0 * qc[1], kf1 * qc[0], kf1 * qc[1]};
+    }
+    float s_raw[4];
+    if (whole && NCOL == 8) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s_raw[e] = sacc[e] * kq[e];
+    } else {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int pos = pos0 + u * TILE + lg + ((e & 2) ? 8 : 0);
-        const bool v = ok[u] && (whole || (pos >= lo && pos < L)) && (2 * lt + (e & 1)) < NCOL;
-        s_raw[u][e] = v ? sacc[u][e] * kq[e] : -INFINITY;
+        const int pos = pos0 + lg + ((e & 2) ? 8 : 0);
+        const bool v = ok && (whole || (pos >= lo && pos < L)) && (2 * lt + (e & 1)) < NCOL;
+        s_raw[e] = v ? sacc[e] * kq[e] : -INFINITY;
       }
     }
 
@@ -840,16 +826,8 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     // warp-uniform) and the V-scale exponent vexp only change when some lane
     // holds a larger value; only then are they reduced over the warp and O
     // and l rescaled, so most tiles take no shuffle here.
-    float lmax[2];
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      float mt = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < PAIR; ++u) mt = fmaxf(mt, fmaxf(s_raw[u][c], s_raw[u][c + 2]));
-      lmax[c] = mt;
-    }
-    bool raise = lmax[0] > m_run[0] || lmax[1] > m_run[1];
-    if constexpr (C::DYN) raise = raise || et_loc > vexp;
+    const float lmax[2] = {fmaxf(s_raw[0], s_raw[2]), fmaxf(s_raw[1], s_raw[3])};
+    const bool raise = lmax[0] > m_run[0] || lmax[1] > m_run[1] || vraise;
     if (__any_sync(0xffffffffu, raise)) {
       float al[2];
 #pragma unroll
@@ -863,7 +841,12 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
         m_run[c] = mn;
       }
       if constexpr (C::DYN) {
-        int et = et_loc;
+        int et = -1000;                 // largest V-scale exponent of the retained rows
+        if (ok) {
+          const int p0 = pos0 + lg, p1 = p0 + 8;
+          if (whole || (p0 >= lo && p0 < L)) et = f32_exp(vs0);
+          if (whole || (p1 >= lo && p1 < L)) et = max(et, f32_exp(vs1));
+        }
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) et = max(et, __shfl_xor_sync(0xffffffffu, et, o));
         const int vnew = max(vexp, max(et, -100));
@@ -873,6 +856,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
           al[1] *= vfix;
           vexp = vnew;
           fv = pow2i(KP - vexp);
+          vcap = pow2i(vexp + 1);
         }
       }
 #pragma unroll
@@ -885,39 +869,27 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
           acc[n][i][3] *= al[1];
         }
     }
-    float pw[PAIR][4];
+    float pw[4];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       // m_run is -inf only while every score so far is -inf: weights 0
       const float mu = (m_run[c] == -INFINITY) ? 0.f : m_run[c];
-      float sum = 0.f;
-#pragma unroll
-      for (int u = 0; u < PAIR; ++u) {
-        pw[u][c] = ex2(s_raw[u][c] - mu);
-        pw[u][c + 2] = ex2(s_raw[u][c + 2] - mu);
-        sum += pw[u][c] + pw[u][c + 2];
-      }
-      l_run[c] += sum;
+      pw[c] = ex2(s_raw[c] - mu);
+      pw[c + 2] = ex2(s_raw[c + 2] - mu);
+      l_run[c] += pw[c] + pw[c + 2];
     }
     // weights that meet V: P' = p v_scale 2^(KP - vexp) (dynamic), p 2^14 (FP8)
     if constexpr (C::DYN) {
-#pragma unroll
-      for (int u = 0; u < PAIR; ++u) {
-        const float f0 = vsr[u][0] * fv, f1 = vsr[u][1] * fv;
-        pw[u][0] *= f0; pw[u][1] *= f0; pw[u][2] *= f1; pw[u][3] *= f1;
-      }
+      const float f0 = vs0 * fv, f1 = vs1 * fv;
+      pw[0] *= f0; pw[1] *= f0; pw[2] *= f1; pw[3] *= f1;
     } else if constexpr (!C::BF) {
 #pragma unroll
-      for (int u = 0; u < PAIR; ++u)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pw[u][e] *= 16384.f;
+      for (int e = 0; e < 4; ++e) pw[e] *= 16384.f;
     }
 
-    // ---------------- PV for each sub-tile
-#pragma unroll
-    for (int u = 0; u < PAIR; ++u) {
-      if (!ok[u]) continue;
-      const float pr[4] = {pw[u][0], pw[u][1], pw[u][2], pw[u][3]};
+    // ---------------- PV
+    if (ok) {
+      const float* pr = pw;
       uint32_t pb[NT][2];
       if constexpr (C::BF) {
 #pragma unroll
@@ -963,36 +935,26 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
           pb[NT - 1][1] = movmatrix_t(live ? l23 : 0u);
         }
       }
-      const uint8_t* vt = kt[u] + C::TBP;
-      const int pb0 = pos0 + u * TILE;
+      const uint8_t* vt = kt + C::TBP;
       if (whole) {
         pv_tile<MODE, D, NT, true>(acc, vt, lg, lt, pb, 0, 0, 0);
       } else {
-        pv_tile<MODE, D, NT, false>(acc, vt, lg, lt, pb, pb0, lo, L);
+        pv_tile<MODE, D, NT, false>(acc, vt, lg, lt, pb, pos0, lo, L);
       }
     }
 
-    // ---------------- advance; refill the consumed stages
-#pragma unroll
-    for (int u = 0; u < PAIR; ++u) {
-      if (u >= cnt) break;
-      seg_klast = cc.k;
-      advance(a, cc);
-    }
+    // ---------------- advance; refill the consumed stage
+    seg_klast = cc.k;
+    advance(a, cc);
     __syncwarp();
-#pragma unroll
-    for (int u = 0; u < PAIR; ++u) {
-      if (u >= cnt) break;
-      if (j + u + NS < ntiles) {
-        fence_proxy_async();
-        issue(cp, blk_next);
-        advance(a, cp);
-        blk_next = block_of(cp);
-      }
+    if (j + NS < ntiles) {
+      fence_proxy_async();
+      issue(cp, blk_next);
+      advance(a, cp);
+      blk_next = block_of(cp);
     }
-    j += cnt;
-    cst += cnt;
-    if (cst >= NS) { cst -= NS; cpar ^= 1u; }
+    ++j;
+    if (++cst == NS) { cst = 0; cpar ^= 1u; }
   }
 
   if (fail_at >= 0) {

@@ -17,6 +17,16 @@ from oracle import oracle as orc
 from tests.helpers import attention_tolerance, bf16_to_f64, bits, check_attention
 
 
+# Workload recipes on which the decode meets the flat max-abs 2e-3 in every
+# mode (measured at full size over every output row).  The Llama-8B-like
+# recipe is not among them: its x32 heads with x8 outlier positions reach
+# outputs of several hundred, where some rows need scores more exact than
+# fp32 holds (tests/test_tolerance_discriminates.py shows that even scores
+# rounded once to fp32 miss 2e-3 there); those rows are held to the per-row
+# bound.
+FLAT_WORKLOADS = {"tiny", "llama70b_128k", "gptoss20b", "gemma_d256"}
+
+
 def K():
     from int4_quantized_paged_gb300 import kvq
     return kvq
@@ -149,14 +159,19 @@ class LayerRun:
             tol[i] = attention_tolerance(qd[b, hq], Kh, Vh, ref[i], 1.0 / np.sqrt(w.D))
         return tol
 
-    def check_decode(self, out, pairs=None, where=""):
+    def check_decode(self, out, pairs=None, where="", flat=None):
+        """Against the oracle: the per-row bound everywhere, and the flat
+        2e-3 too when `flat` (default: the workload is one measured to meet
+        it, see FLAT_WORKLOADS)."""
         w = self.w
         if pairs is None:
             pairs = [(b, h) for b in range(w.B) for h in range(w.Hq)]
         ref = self.oracle_decode(pairs)
         got = out.cpu().numpy()[[p[0] for p in pairs], [p[1] for p in pairs]]
         tol = self.tolerance(ref, pairs)
-        return check_attention(got, ref, tol, where or f"{w.name} mode {self.mode}")
+        if flat is None:
+            flat = w.name in FLAT_WORKLOADS
+        return check_attention(got, ref, tol, where or f"{w.name} mode {self.mode}", flat=flat)
 
 
 def _rows(mode, codes, slot_scales, static, blk, g, off):

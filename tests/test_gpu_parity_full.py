@@ -14,10 +14,12 @@ from a plain GPU run:
 
     KVQ_PARITY_REPORT=parity.jsonl python -m pytest tests/test_gpu_parity_full.py -m gpu
 
-Cases in FLAT assert the flat 2e-3 on every element.  The others (heads whose
-scores and values reach the hundreds, where 2e-3 is below what fp32 can
-resolve, see tests/helpers.attention_tolerance) assert the flat bound on every
-row that meets it and the per-row fp32 forward-error bound on the rest.
+Workloads in tests.gpu_harness.FLAT_WORKLOADS assert the flat 2e-3 on every
+element.  The Llama-8B-like recipe (x32 heads with x8 outlier positions,
+outputs of several hundred, where some rows need scores more exact than fp32
+holds: tests/test_tolerance_discriminates.py) asserts the flat bound on every
+row that meets it and the per-row fp32 forward-error bound of
+tests/helpers.attention_tolerance on the rest.
 """
 import json
 import os
@@ -28,7 +30,7 @@ import torch
 
 from int4_quantized_paged_gb300 import workloads as wl
 from oracle import oracle as orc
-from tests.gpu_harness import LayerRun
+from tests.gpu_harness import FLAT_WORKLOADS, LayerRun
 from tests.helpers import check_attention
 
 pytestmark = pytest.mark.gpu
@@ -57,9 +59,6 @@ CASES = [
     ("gemma-win-int4", "gemma_d256", orc.INT4_PER_TOKEN_HEAD, 0),
     ("gemma-full-int4", "gemma_d256", orc.INT4_PER_TOKEN_HEAD, 1),
 ]
-
-# Cases measured to meet the flat 2e-3 on every element.
-FLAT = set()
 
 
 def _record(row):
@@ -94,7 +93,7 @@ def test_full_size_every_row(case, name, mode, layer):
         rec["max_abs_ref_in_rows_over"] = float(np.abs(ref[over]).max())
     _record(rec)
     assert rel <= REL_L2, f"{case}: relative L2 {rel:.3e}"
-    if case in FLAT:
+    if name in FLAT_WORKLOADS:
         assert len(over) == 0, f"{case}: {rec['elements_over_2e-3']} elements over 2e-3, " \
                                f"worst {rec['max_abs_err']:.3e}"
     elif len(over):

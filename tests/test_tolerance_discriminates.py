@@ -120,3 +120,43 @@ def test_f16_scores_are_rejected(case):
     out, tol = _decode(case, score_round=_f16, weight_split=_f16_hi_lo)
     with pytest.raises(AssertionError, match="over tolerance|relative L2"):
         check_attention(out, case["ref"], tol, "scores rounded to f16")
+
+
+def test_flat_bound_is_beyond_fp32_scores_on_the_full_llama8b_recipe():
+    """Why the Llama-8B-like rows are held to the per-row bound and not the
+    flat 2e-3: on the full workload (64 sequences x 4096 positions), a decode
+    whose only rounding is each score rounded once to fp32 (everything else
+    float64) already misses 2e-3 on some rows, where near-tied scores of
+    several hundred select values of several hundred.  No kernel with fp32
+    scores can do better.  The per-row bound accepts it."""
+    w = wl.CONFIGS["llama8b"]
+    fill = host_fill(w)
+    mode = orc.FP8_PER_TOKEN_HEAD
+    pg = fill["paging"]
+    kc, vc, ks, vs = orc.alloc_cache(mode, pg.num_blocks, w.Hkv, w.block_size, w.D)
+    orc.cache_write(mode, fill["k_bits"], fill["v_bits"], fill["slots_np"], kc, vc, ks, vs)
+    qd = bf16_to_f64(bits(wl.queries(w, "cpu")))
+    Kh = orc.dequantize(mode, kc, ks)
+    Vh = orc.dequantize(mode, vc, vs)
+    bt, bs = fill["block_table"], w.block_size
+    scale = 1.0 / np.sqrt(w.D)
+    worst, rows_over = 0.0, 0
+    for b in range(w.B):
+        p = np.arange(int(fill["context_lens"][b]))
+        blk, off = bt[b, p // bs], p % bs
+        for g in range(w.Hkv):
+            K, V = Kh[blk, g, off], Vh[blk, g, off]
+            for j in range(w.G):
+                q = qd[b, g * w.G + j]
+                s = (K @ q) * scale
+                e = np.exp(s - s.max())
+                ref = (e @ V) / e.sum()
+                s32 = s.astype(np.float32).astype(np.float64)
+                e32 = np.exp(s32 - s32.max())
+                got = (e32 @ V) / e32.sum()
+                err = np.abs(got - ref)
+                if err.max() > 2e-3:
+                    rows_over += 1
+                    assert np.all(err <= attention_tolerance(q, K, V, ref, scale))
+                worst = max(worst, float(err.max()))
+    assert rows_over > 0 and worst > 2e-3
