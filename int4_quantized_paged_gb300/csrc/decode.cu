@@ -970,23 +970,21 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
   finalize();
 }
 
-// Log-sum-exp merge: one CTA per (sequence, KV head) item, one warp per
-// (query head, 32-element slice of D), each lane one element of the slice.
-// Items covered by one worker (or by none) were written by the decode kernel;
-// the others combine the partials of their workers.  A warp loads the (m, l)
-// pairs of up to 32 workers at once and keeps eight partial elements in
-// flight per lane, so even an item split over dozens of workers costs a few
-// dependent rounds of loads after the item offsets.
+// Log-sum-exp merge: one CTA per (sequence, KV head) item, one warp per query
+// head of the group.  Items covered by one worker (or by none) were written by
+// the decode kernel; the others combine the partials of their workers.  The
+// partial rows of the first PRE workers are loaded together with the (m, l)
+// pairs, so an item split over at most PRE workers costs two dependent rounds
+// of loads after the item offsets.
 template <int D, int G>
-__global__ void __launch_bounds__(G * D) merge_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(32 * G) merge_kernel(const DecodeArgs a) {
   // launched as a programmatic dependent of the decode kernel: wait until that
   // grid has completed and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  constexpr int U = 8;                                  // partial loads in flight per lane
+  constexpr int PRE = 8;
+  constexpr int DL = D / 32;                            // elements per lane
   const int item = blockIdx.x;
-  const int wrp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = wrp / (D / 32);                         // query head within the group
-  const int d = (wrp % (D / 32)) * 32 + lane;           // this lane's element
+  const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long P = a.item_tiles[item], n = a.item_tiles[item + 1] - P;
   const long long T = a.item_tiles[(long long)a.B * a.Hkv];
   if (n <= 0) return;
@@ -996,10 +994,21 @@ __global__ void __launch_bounds__(G * D) merge_kernel(const DecodeArgs a) {
   if (w0 == w1) return;
   const int b = item / a.Hkv, g = item - b * a.Hkv;
   // a worker whose share is empty (more workers than tiles) wrote nothing, and
-  // its slot may hold anything: such workers get weight 0 and are skipped
+  // its slot may hold anything: such workers get weight 0 and are selected out
   auto live_w = [&](long long w) { return w <= w1 && (w * T) / W != ((w + 1) * T) / W; };
-  float acc = 0.f, M = -INFINITY, lsum = 0.f;
-  // chunks of 32 workers: lane w - c0 holds that worker's (m, l)
+  auto row = [&](long long w) { return a.ws_o + ((item + w) * G + j) * D; };
+  float pre[PRE][DL];
+#pragma unroll
+  for (int u = 0; u < PRE; ++u) {
+    const long long w = (w0 + u <= w1) ? w0 + u : w0;
+#pragma unroll
+    for (int k = 0; k < DL; ++k) pre[u][k] = row(w)[lane + 32 * k];
+  }
+  float acc[DL];
+#pragma unroll
+  for (int k = 0; k < DL; ++k) acc[k] = 0.f;
+  float M = -INFINITY, lsum = 0.f;
+  // chunks of 32 workers: lane w-c0 holds that worker's (m, l)
   for (long long c0 = w0; c0 <= w1; c0 += 32) {
     const long long w = c0 + lane;
     float m = -INFINITY, l = 0.f;
@@ -1019,27 +1028,48 @@ __global__ void __launch_bounds__(G * D) merge_kernel(const DecodeArgs a) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
     lsum = lsum * rescale + ls;
-    acc *= rescale;
-    M = Mn;
-    const int cnt = (int)min(32LL, w1 - c0 + 1);
-    for (int i0 = 0; i0 < cnt; i0 += U) {
-      float v[U], fi[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        // missing ones read slot c0 and get weight 0
-        const int i = (i0 + u < cnt) ? i0 + u : 0;
-        fi[u] = __shfl_sync(0xffffffffu, f, i);
+    for (int k = 0; k < DL; ++k) acc[k] *= rescale;
+    const int cnt = (int)min(32LL, w1 - c0 + 1);
+    int i0 = 0;
+    if (c0 == w0) {
+      // the prefetched rows
+#pragma unroll
+      for (int u = 0; u < PRE; ++u) {
+        const float fu = (u < cnt) ? __shfl_sync(0xffffffffu, f, u) : 0.f;
+#pragma unroll
+        for (int k = 0; k < DL; ++k) acc[k] = fu != 0.f ? fmaf(fu, pre[u][k], acc[k]) : acc[k];
+      }
+      i0 = PRE;
+    }
+    for (; i0 < cnt; i0 += 4) {
+      // four partials' loads in flight at once; missing ones read slot c0
+      float v[4][DL], fi[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        fi[u] = __shfl_sync(0xffffffffu, f, (i0 + u) & 31);
+        const long long ii = (i0 + u < cnt) ? i0 + u : 0;
         if (i0 + u >= cnt) fi[u] = 0.f;
-        v[u] = a.ws_o[((item + c0 + i) * G + j) * D + d];
+#pragma unroll
+        for (int k = 0; k < DL; ++k) v[u][k] = row(c0 + ii)[lane + 32 * k];
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) acc = fi[u] != 0.f ? fmaf(fi[u], v[u], acc) : acc;
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int k = 0; k < DL; ++k) acc[k] = fi[u] != 0.f ? fmaf(fi[u], v[u][k], acc[k]) : acc[k];
     }
+    M = Mn;
   }
-  const long long o = ((long long)b * a.Hq + g * G + j) * D + d;
-  const float r = lsum > 0.f ? acc / lsum : 0.f;
-  if (a.out_bf16) a.out_bf16[o] = (uint16_t)(pack_bf16x2(r, 0.f) & 0xFFFFu);
-  else a.out[o] = r;
+  const long long orow = ((long long)b * a.Hq + g * G + j) * D;
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  if (a.out_bf16) {
+#pragma unroll
+    for (int k = 0; k < DL; ++k)
+      a.out_bf16[orow + lane + 32 * k] = (uint16_t)(pack_bf16x2(acc[k] * inv, 0.f) & 0xFFFFu);
+  } else {
+#pragma unroll
+    for (int k = 0; k < DL; ++k) a.out[orow + lane + 32 * k] = acc[k] * inv;
+  }
 }
 
 // ------------------------------------------------------------------ host
@@ -1086,7 +1116,7 @@ cudaError_t launch3(const DecodeArgs& a, cudaStream_t st) {
   // decode grid's tail
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(a.B * a.Hkv));
-  cfg.blockDim = dim3(G * D);
+  cfg.blockDim = dim3(32 * G);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

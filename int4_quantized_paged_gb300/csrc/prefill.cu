@@ -1,4 +1,5 @@
-// Prefill (chunked multi-query) attention over the quantized paged cache.
+// Prefill (chunked multi-query) attention over the quantized paged cache on
+// the fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // What it computes: sequence b appends n_b tokens at positions
 // [L_b - n_b, L_b) (their K/V already written by the cache write); each new
@@ -10,25 +11,38 @@
 // FP8 KV cache scales", section "Use a three-stage decision").
 //
 // Work decomposition (one CTA per query tile, no split of the keys):
-//  * A CTA owns ROWS = 128 query rows of one (sequence, KV head): QP = 128/G
+//  * A CTA owns M = 128 query rows of one (sequence, KV head): 128/G
 //    consecutive new positions times the G query heads of that KV head, so a
 //    key/value tile is fetched and dequantized once for all of them.  CTAs
 //    with the latest (longest) query tiles start first.
-//  * Keys stream in tiles of 64 positions (four 16-position page tiles, one
-//    2-D TMA box each for K and V, plus 64-byte bulk copies of the dynamic
-//    scales) through NSR raw stages.  After each tile lands, all threads
-//    convert it once into f16 (bf16 for BF16 layers) shared-memory tiles K16
-//    and V16 (exact: E4M3 and INT4 codes are f16 values); positions outside
-//    the CTA's key range become zeros, so no stale byte reaches a product.
-//  * Eight warps, each 16 rows, in FlashAttention-2 layout on mma.m16n8k16:
-//    S = Q K^T with Q and K fragments from ldmatrix, the online softmax on
-//    the accumulators (log2 units, causal and window masks per row), and
-//    O += P' V with the S accumulators reused as the A fragments and V
-//    fragments from ldmatrix.trans.  P' = p x v_scale x 2^k as in decode
-//    (k a power-of-two range factor per warp), split into f16 hi + lo (three
-//    bf16 terms for BF16 layers) so the weights keep fp32-class accuracy.
-//  * q is prescaled per row by a power of two so its bf16 values are exact
-//    in f16; the factor returns on the score.
+//  * Keys stream in tiles of KT positions (64; 32 for BF16 at D = 256, whose
+//    pages are largest): KT/16 page tiles by 2-D TMA for K and V plus 64-byte
+//    bulk copies of the dynamic scales, through NSR raw stages.  All threads
+//    convert a landed tile once into f16 (bf16 for BF16 layers; exact) in the
+//    tensor cores' shared-memory layout: K as KT rows of D (K-major, 128-byte
+//    swizzle) and V transposed, D rows of KT keys, through a row-major
+//    staging copy.  Positions outside the CTA's key range become zeros.
+//  * S = Q K^T: one thread issues D/16 tcgen05.mma (M 128, N KT, K 16) from
+//    shared-memory descriptors into KT tensor-memory columns, and commits them
+//    to a shared-memory barrier.
+//  * Softmax: every warp takes 32 query rows (its tensor-memory lanes) and one
+//    half of the tile's keys; a thread loads its row's KT/2 scores
+//    (tcgen05.ld), applies the K scale and, on tiles not wholly visible to
+//    every row, the causal / window masks, and the two halves exchange their
+//    maxima through shared memory.  The row's reference max moves only when
+//    a tile exceeds it by more than 2^8 (log2 units 8), so the output
+//    accumulator in tensor memory is rescaled rarely (each half rescales its
+//    half of the columns); the weights stay below 2^8 and meet V as
+//    P' = p x v_scale x 2^k (k keeps P' below 2^15), split into f16 hi + lo
+//    (three bf16 terms for BF16 layers) and written to shared memory, K-major.
+//  * O += P' V: one thread issues the split's terms (M 128, N D, K 16 each)
+//    into D tensor-memory columns and commits.  The next tile's conversion
+//    waits for that commit before it overwrites the operands.
+//  * Epilogue: each thread reads its half of its row of O (tcgen05.ld),
+//    divides by the row sum (both halves' sums) and stores fp32.  Tensor memory is allocated and freed
+//    by warp 0; every wait is bounded, and a wait that runs out flags TIMEOUT,
+//    lets the work already issued finish (bounded again) and frees tensor
+//    memory before the CTA exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -41,42 +55,145 @@
 namespace kvq {
 namespace {
 
-constexpr int PWARPS = 8;                  // warps per CTA
-constexpr int ROWS = 16 * PWARPS;          // query rows per CTA
-constexpr int KT = 64;                     // key positions per tile
-constexpr int SUB = KT / 16;               // 16-position page tiles per key tile
-constexpr int PKP = 13;                    // P' = p v_scale 2^(PKP - vexp) < 2^14
+constexpr int TWARPS = 8;                  // warps per CTA
+constexpr int TROWS = 128;                 // query rows per CTA (the MMA's M)
+constexpr int TKP = 6;                     // P' = p v_scale 2^(TKP - vexp) < 2^15 (p <= 2^8)
+constexpr float TLAZY = 8.f;               // the row's reference max moves when exceeded by this
+constexpr float TSTATIC = 64.f;            // P' = p x 64 for static FP8 scales (< 2^14)
 
-__device__ __forceinline__ void ldsm_x4(uint32_t r[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
+// ------------------------------------------------------------ tcgen05 wrappers
+// Shared-memory matrix descriptor of a K-major operand in the canonical
+// 128-byte-swizzle layout: rows of 128 bytes (64 f16 of K), 8-row groups 1024
+// bytes apart, 16-byte chunk c of row r stored at chunk c ^ (r & 7).  The
+// start address may be advanced by 32-byte steps along K inside a row.
+__device__ __forceinline__ uint64_t sw128_desc(const void* p) {
+  const uint32_t a = smem_u32(p);
+  uint64_t d = (uint64_t)((a >> 4) & 0x3FFFu);      // start address / 16
+  d |= (uint64_t)1 << 16;                            // leading offset (unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;                  // stride between 8-row groups
+  d |= (uint64_t)1 << 46;                            // descriptor version
+  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+  return d;
 }
 
-__device__ __forceinline__ void ldsm_x4_t(uint32_t r[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
+// Instruction descriptor: f32 accumulator, f16 (BF false) or bf16 operands,
+// both K-major, M x N.
+template <bool BF>
+__host__ __device__ constexpr uint32_t mma_idesc(int M, int N) {
+  return (1u << 4) | ((BF ? 1u : 0u) << 7) | ((BF ? 1u : 0u) << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
+                                     bool accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
+      "l"(da), "l"(db), "r"(idesc), "r"((uint32_t)accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Byte offset of 16-byte chunk `c` of row `r` in a 128-byte-swizzled block.
+__device__ __forceinline__ uint32_t swc(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------------ configuration
 template <int MODE, int D>
-struct PCfg {
+struct TCfg {
   static constexpr int RB = row_bytes<MODE>(D);
   static constexpr int TB = 16 * RB;                       // one page tile (16 positions)
   static constexpr int TBP = (TB + 1023) / 1024 * 1024;
   static constexpr bool DYN = (MODE == FP8_PER_TOKEN_HEAD || MODE == INT4_PER_TOKEN_HEAD);
   static constexpr bool BF = (MODE == BF16);
+  static constexpr int KT = (BF && D == 256) ? 32 : 64;    // keys per tile
+  static constexpr int SUB = KT / 16;                       // page tiles per key tile
+  static constexpr int NPART = BF ? 3 : 2;                  // terms of the P' split
   static constexpr int RAW = 2 * SUB * TBP;                 // K and V page tiles of a key tile
   static constexpr int SCB = DYN ? 2 * SUB * 64 : 0;        // their K and V scales
-  static constexpr int LD = D + 8;                          // f16 row pitch (elements)
-  static constexpr int KV16 = KT * LD * 2;                  // bytes of K16 (and of V16)
-  static constexpr int Q16 = ROWS * LD * 2;
-  static constexpr int FIXED = 2 * KV16 + Q16 + 2 * KT * 4 + ROWS * 8 + 64;
-  // raw stages: two where they fit beside the rest in 227 KB, else one
-  static constexpr int NSR = (2 * (RAW + SCB) + FIXED + 2048 <= 232448) ? 2 : 1;
-  static constexpr int RAWS = (RAW + SCB + 1023) / 1024 * 1024;   // stage pitch
-  static constexpr int SMEM = NSR * RAWS + FIXED + 1024;           // + alignment slack
-  static constexpr int NPART = BF ? 3 : 2;                  // terms of the P' split
+  static constexpr int RAWS = (RAW + SCB + 1023) / 1024 * 1024;
+  static constexpr int QB = TROWS * D * 2;                  // Q: D/64 blocks of 128 x 128 B
+  static constexpr int KB = KT * D * 2;                     // K: D/64 blocks of KT x 128 B
+  static constexpr int VTB = D * 128;                       // V^T: D rows of 128 B (KT keys)
+  static constexpr int PB = TROWS * 128;                    // one P' term: 128 rows of 128 B
+  static constexpr int LDV = (D + 8) * 2;                   // row pitch (bytes) of the V staging copy
+  // the P' terms' region, which also holds the V staging copy during conversion
+  static constexpr int PREG = (NPART * PB > KT * LDV) ? NPART * PB : KT * LDV;
+  // the operands of one key tile: K, V^T and the P' region
+  static constexpr int BUF = (KB + VTB + PREG + 1023) / 1024 * 1024;
+  // K and V scales and the tile's V-scale exponents
+  static constexpr int SCB1 = 2 * KT * 4 + 16;
+  // row data, per-half row maxima / sums, barriers, flags
+  static constexpr int SMALLC = TROWS * 8 + 2 * TROWS * 4 + 128;
+  static constexpr int LIMIT = 232448 - 1024;               // per-CTA shared memory, minus slack
+  static constexpr int FIXED = QB + BUF + SCB1 + SMALLC;
+  static constexpr int NSR = (2 * RAWS + FIXED <= LIMIT) ? 2 : 1;
+  static constexpr int SMEM = NSR * RAWS + FIXED + 1024;
+  static constexpr int OCOL = KT;                           // S: [0, KT), O: [KT, KT + D)
+  static constexpr int TCOLS = (OCOL + D <= 128) ? 128 : ((OCOL + D <= 256) ? 256 : 512);
 };
 
 struct PrefillArgs {
@@ -85,34 +202,73 @@ struct PrefillArgs {
   int qtiles;                    // query tiles per (sequence, KV head) in the grid
 };
 
+// 16 raw code bytes -> their f16 (bf16 for BF16) values: 8 (BF16), 16 (FP8)
+// or 32 (INT4) elements, as 1, 2 or 4 16-byte chunks.  Exact.
+template <int MODE>
+__device__ __forceinline__ void convert16(uint4 w, uint4 (&o)[4]) {
+  if constexpr (MODE == BF16) {
+    o[0] = w;
+  } else if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t x = ws[q];
+      // low nibble of byte j = element 2j: e = {b0.lo, b1.lo}, h = 16 {b0.hi, b1.hi}
+      const uint32_t e0 = nib2_f16x2<0>(__byte_perm(x, 0u, 0x7170));
+      const uint32_t h0 = nib2_f16x2<1>(__byte_perm(x, 0u, 0x7170));
+      const uint32_t e1 = nib2_f16x2<0>(__byte_perm(x, 0u, 0x7372));
+      const uint32_t h1 = nib2_f16x2<1>(__byte_perm(x, 0u, 0x7372));
+      uint32_t hs0, hs1;
+      asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hs0) : "r"(h0), "r"(0x2C002C00u));   // x 1/16
+      asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hs1) : "r"(h1), "r"(0x2C002C00u));
+      o[q].x = __byte_perm(e0, hs0, 0x5410);
+      o[q].y = __byte_perm(e0, hs0, 0x7632);
+      o[q].z = __byte_perm(e1, hs1, 0x5410);
+      o[q].w = __byte_perm(e1, hs1, 0x7632);
+    }
+  } else {
+    e4m3x4_f16(w.x, o[0].x, o[0].y);
+    e4m3x4_f16(w.y, o[0].z, o[0].w);
+    e4m3x4_f16(w.z, o[1].x, o[1].y);
+    e4m3x4_f16(w.w, o[1].z, o[1].w);
+  }
+}
+
 template <int MODE, int D, int G>
-__global__ void __launch_bounds__(PWARPS * 32, 1)
-    prefill_kernel(const PrefillArgs pa, const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap) {
-  using C = PCfg<MODE, D>;
+__global__ void __launch_bounds__(TWARPS * 32, 1)
+    prefill_tc_kernel(const PrefillArgs pa, const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap) {
+  using C = TCfg<MODE, D>;
   using ET = uint16_t;
   const DecodeArgs& a = pa.d;
-  constexpr int QP = ROWS / G;                 // positions per query tile
-  constexpr int LD = C::LD;
+  constexpr int KT = C::KT;
+  constexpr int SUB = C::SUB;
   constexpr int NSR = C::NSR;
-  constexpr int NT = D / 8;                    // O n-tiles (8 d values each)
+  constexpr int QP = TROWS / G;                // positions per query tile
+  constexpr int CPR = C::RB / 16;              // 16-byte raw chunks per position row
+  constexpr int EPC = (MODE == BF16) ? 8 : (MODE == INT4_PER_TOKEN_HEAD ? 32 : 16);  // elements per raw chunk
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* raw = smem;                                       // NSR stages
-  ET* k16 = reinterpret_cast<ET*>(smem + NSR * C::RAWS);
-  ET* v16 = k16 + KT * LD;
-  ET* q16 = v16 + KT * LD;
-  float* ksm = reinterpret_cast<float*>(q16 + ROWS * LD);    // [KT] K scale (0: no key)
+  uint8_t* q16 = smem + NSR * C::RAWS;                       // Q, K-major swizzled
+  uint8_t* k16 = q16 + C::QB;                                // K, K-major swizzled
+  uint8_t* vt16 = k16 + C::KB;                               // V^T, K-major swizzled
+  uint8_t* p16 = vt16 + C::VTB;                              // P' terms; also the V staging copy
+  float* ksm = reinterpret_cast<float*>(k16 + C::BUF);      // [KT] K scale (0: no key)
   float* vsm = ksm + KT;                                     // [KT] V scale
-  float* rowf = vsm + KT;                                    // [ROWS] score factor per row
-  int* rowp = reinterpret_cast<int*>(rowf + ROWS);           // [ROWS] position (-1: no row)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rowp + ROWS); // [NSR]
-  __shared__ int s_flag;
+  int* etile = reinterpret_cast<int*>(vsm + KT);             // [4] tile V-scale exponents
+  float* rowf = reinterpret_cast<float*>(etile + 4);         // [TROWS] score factor per row
+  int* rowp = reinterpret_cast<int*>(rowf + TROWS);          // [TROWS] position (-1: no row)
+  float* mx = reinterpret_cast<float*>(rowp + TROWS);       // [2][TROWS] per-half row max / sum
+  uint64_t* bars = reinterpret_cast<uint64_t*>(mx + 2 * TROWS);  // [NSR] raw, then S, then O
+  uint64_t* bar_s = bars + NSR;
+  uint64_t* bar_o = bar_s + 1;
+  int& s_flag = *reinterpret_cast<int*>(bar_o + 1);
+  uint32_t& s_tmem = *(reinterpret_cast<uint32_t*>(bar_o + 1) + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int lg = lane >> 2, lt = lane & 3;
 
   // ---- this CTA's (sequence, KV head, query tile); latest tiles first
   const int per_tile = a.B * a.Hkv;
@@ -121,7 +277,7 @@ __global__ void __launch_bounds__(PWARPS * 32, 1)
   const int b = rem / a.Hkv, g = rem - b * a.Hkv;
   const int q0 = pa.query_start[b];
   const int n_b = pa.query_start[b + 1] - q0;
-  int L = a.context_lens[b];
+  const int L = a.context_lens[b];
   if (qt * QP >= n_b || n_b <= 0) return;                   // whole CTA: before any barrier
   // the chunk cannot start before 0, and its last position must lie inside
   // the positions the sequence's block-table row covers
@@ -136,17 +292,24 @@ __global__ void __launch_bounds__(PWARPS * 32, 1)
   const int t0 = kmin / KT, t1 = pmax / KT;                 // key tiles, inclusive
 
   if (tid == 0) {
-    for (int s = 0; s < NSR; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < NSR + 2; ++s) mbar_init(&bars[s], 1);
     mbar_init_fence();
     s_flag = 0;
   }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&s_tmem)),
+                 "r"(C::TCOLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
 
-  // ---- queries: row r = h * QP + i -> token q0 + qt*QP + i, head g*G + h.
-  // Warp w stages rows w, w + 8, ...: one row per pass, D/32 elements a lane.
+  // ---- queries: row r = h * QP + i -> token q0 + qt*QP + i, head g*G + h,
+  // prescaled by a power of two so the bf16 values are exact in f16.  Warp w
+  // stages rows w, w + 8, ...; lane l holds elements l + 32e.
   float ks_static = 1.f;
   if constexpr (MODE == FP8_PER_TENSOR) ks_static = a.k_scale[0];
   if constexpr (MODE == FP8_PER_HEAD) ks_static = a.k_scale[g];
-  for (int r = warp; r < ROWS; r += PWARPS) {
+  for (int r = warp; r < TROWS; r += TWARPS) {
     const int h = r / QP, i = r - h * QP;
     const bool valid = i < nq;
     constexpr int EL = D / 32;
@@ -170,16 +333,21 @@ __global__ void __launch_bounds__(PWARPS * 32, 1)
     const float qmul = C::BF ? 1.f : pow2i(14 - qexp);
 #pragma unroll
     for (int e = 0; e < EL; ++e) {
+      const int d = lane + 32 * e;
       const float v = x[e] * qmul;
-      q16[r * LD + lane + 32 * e] =
-          C::BF ? (uint16_t)(pack_bf16x2(v, 0.f) & 0xFFFFu) : (uint16_t)(pack_f16x2(v, 0.f) & 0xFFFFu);
+      const ET h16 = C::BF ? (ET)(pack_bf16x2(v, 0.f) & 0xFFFFu) : (ET)(pack_f16x2(v, 0.f) & 0xFFFFu);
+      *reinterpret_cast<ET*>(q16 + (d >> 6) * (TROWS * 128) + swc(r, (d & 63) >> 3) + (d & 7) * 2) = h16;
     }
     if (lane == 0) {
       rowf[r] = a.qk_scale * ks_static * (C::BF ? 1.f : pow2i(qexp - 14));
       rowp[r] = valid ? first + i : -1;
     }
   }
+  fence_proxy_async();
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
 
   // ---- copies of key tile t into raw stage st: warp 0, lane s < SUB takes
   // page tile s.  Page tiles wholly outside [kmin, pmax] are not fetched.
@@ -217,276 +385,337 @@ __global__ void __launch_bounds__(PWARPS * 32, 1)
     return fetch;
   };
   unsigned fetched[2] = {0u, 0u};                  // page tiles fetched per stage (warp 0)
+  int pend[2] = {-1, -1};                          // tile issued into each stage, not yet landed
   if (warp == 0)
-    for (int s = 0; s < NSR && t0 + s <= t1; ++s) fetched[s] = issue(t0 + s, s);
+    for (int s = 0; s < NSR && t0 + s <= t1; ++s) {
+      fetched[s] = issue(t0 + s, s);
+      pend[s] = t0 + s;
+    }
 
-  // ---- per-warp state: rows rA = 16 warp + lg and rB = rA + 8
-  const int rA = 16 * warp + lg, rB = rA + 8;
-  const int pA = rowp[rA], pB = rowp[rB];
+  // ---- softmax state.  Every warp scores half of each key tile for 32 rows:
+  // warp w takes rows (w & 3) * 32 + lane (its tensor-memory lanes) and keys
+  // [half * KH, half * KH + KH) with half = w >> 2.
+  constexpr int KH = KT / 2;
+  const int r = (warp & 3) * 32 + lane;
+  const int half = warp >> 2;
+  const int pA = rowp[r];
   const int loA = (a.window > 0) ? max(0, pA + 1 - a.window) : 0;
-  const int loB = (a.window > 0) ? max(0, pB + 1 - a.window) : 0;
-  const float fA = rowf[rA], fB = rowf[rB];
-  float acc[NT][4];
-#pragma unroll
-  for (int n = 0; n < NT; ++n)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
-  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+  const float fA = rowf[r];
+  const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  // mU: the row's reference max (log2 units) the weights are taken against;
+  // it moves only when a tile's max exceeds it by more than TLAZY, so the
+  // output accumulator is rescaled rarely and the weights stay below 2^TLAZY
+  float mU = -INFINITY, lH = 0.f;                  // lH: this half's running sum
   int vexp = -1000;
-  float fv = 0.f;                                  // 2^(PKP - vexp)
+  float fv = 0.f;                                  // 2^(TKP - vexp)
   float vs_static = 1.f;
   if constexpr (MODE == FP8_PER_TENSOR) vs_static = a.v_scale[0];
   if constexpr (MODE == FP8_PER_HEAD) vs_static = a.v_scale[g];
+  constexpr uint32_t IDS = mma_idesc<C::BF>(TROWS, KT);
+  constexpr uint32_t IDO = mma_idesc<C::BF>(TROWS, D);
 
-  for (int t = t0; t <= t1; ++t) {
-    const int st = (t - t0) % NSR;
-    const uint32_t par = (uint32_t)(((t - t0) / NSR) & 1);
-    const bool ok = mbar_wait(&bars[st], par);
-    if (__syncthreads_or(!ok)) {
-      // a copy never completed: flag it, let the other stage's copies land
-      // (bounded), and stop
-      if (tid == 0) {
-        atomicOr(a.err, ERR_TIMEOUT);
-        if (NSR == 2 && t + 1 <= t1)
-          (void)mbar_wait(&bars[st ^ 1], (uint32_t)(((t + 1 - t0) / NSR) & 1));
-      }
-      return;
-    }
+  bool failed = false;
+  int issued_s = 0, issued_o = 0;                  // S and PV commits issued (barrier phases)
+  unsigned have = 0u;                              // fetched pages of the current key tile
+
+  // Waits for key tile tt's pages and for the last PV (the previous reader of
+  // K, V^T and P'), converts the tile and issues S = Q K^T.
+  auto convert_and_score = [&](int tt) -> bool {
+    const int st = (tt - t0) % NSR;
+    const uint32_t par = (uint32_t)(((tt - t0) / NSR) & 1);
+    bool ok = mbar_wait(&bars[st], par);
+    if (issued_o > 0) ok = mbar_wait(bar_o, (uint32_t)((issued_o - 1) & 1)) && ok;
+    if (__syncthreads_or(!ok)) return false;
+    pend[st] = -1;
+    tc_fence_after();
     // which page tiles of this key tile hold data (warp 0 knows; share it)
     if (tid == 0) s_flag = (int)fetched[st];
     __syncthreads();
-    const unsigned have = (unsigned)s_flag;
+    have = (unsigned)s_flag;
     const uint8_t* base = raw + st * C::RAWS;
-    // ---- convert the tile into K16 / V16 (zeros where nothing was fetched or
-    // the position lies outside [kmin, pmax]); scales into ksm / vsm
-    {
-      constexpr int CH = C::RB / 16;               // 16-byte chunks per position row
-      for (int c = tid; c < 2 * KT * CH; c += PWARPS * 32) {
-        const int isv = c >= KT * CH;
-        const int cc = isv ? c - KT * CH : c;
-        const int key = cc / CH, ch = cc - key * CH;
-        const int sub = key >> 4, kr = key & 15;
-        const int pos = t * KT + key;
-        const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (live)
-          w = *reinterpret_cast<const uint4*>(base + (isv ? SUB + sub : sub) * C::TBP +
-                                             swz((uint32_t)(kr * C::RB + ch * 16)));
-        ET* dst = (isv ? v16 : k16) + key * LD;
-        if constexpr (MODE == BF16) {
-          *reinterpret_cast<uint4*>(dst + ch * 8) = w;
-        } else if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
-          // 32 nibbles -> 32 f16 (exact): low nibble of byte j = element 2j
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint8_t* kb = k16;
+    uint8_t* pb = p16;
+    // K into kb, V into the row-major staging copy in pb (zeros where
+    // nothing was fetched or the position lies outside [kmin, pmax])
+    for (int c = tid; c < 2 * KT * CPR; c += TWARPS * 32) {
+      const int isv = c >= KT * CPR;
+      const int cc = isv ? c - KT * CPR : c;
+      const int key = cc / CPR, ch = cc - key * CPR;
+      const int sub = key >> 4, kr = key & 15;
+      const int pos = tt * KT + key;
+      const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (live)
+        w = *reinterpret_cast<const uint4*>(base + (isv ? SUB + sub : sub) * C::TBP +
+                                           swz((uint32_t)(kr * C::RB + ch * 16)));
+      uint4 o[4];
+      convert16<MODE>(w, o);
+      constexpr int NCH = EPC / 8;                 // output chunks of 8 elements
+      const int d0 = ch * EPC;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t x = ws[q];
-            const uint32_t e0 = nib2_f16x2<0>(__byte_perm(x, 0u, 0x7170));   // bytes 0,1 low
-            const uint32_t h0 = nib2_f16x2<1>(__byte_perm(x, 0u, 0x7170));   // bytes 0,1 high x16
-            const uint32_t e1 = nib2_f16x2<0>(__byte_perm(x, 0u, 0x7372));
-            const uint32_t h1 = nib2_f16x2<1>(__byte_perm(x, 0u, 0x7372));
-            // e0 = {b0.lo, b1.lo}, h0 = 16 {b0.hi, b1.hi}: order b0.lo b0.hi b1.lo b1.hi
-            uint32_t hs0, hs1;
-            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hs0) : "r"(h0), "r"(0x2C002C00u));   // x 1/16
-            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hs1) : "r"(h1), "r"(0x2C002C00u));
-            uint4 o;
-            o.x = __byte_perm(e0, hs0, 0x5410);
-            o.y = __byte_perm(e0, hs0, 0x7632);
-            o.z = __byte_perm(e1, hs1, 0x5410);
-            o.w = __byte_perm(e1, hs1, 0x7632);
-            *reinterpret_cast<uint4*>(dst + ch * 32 + 8 * q) = o;
-          }
-        } else {
-          uint4 o0, o1;
-          e4m3x4_f16(w.x, o0.x, o0.y);
-          e4m3x4_f16(w.y, o0.z, o0.w);
-          e4m3x4_f16(w.z, o1.x, o1.y);
-          e4m3x4_f16(w.w, o1.z, o1.w);
-          *reinterpret_cast<uint4*>(dst + ch * 16) = o0;
-          *reinterpret_cast<uint4*>(dst + ch * 16 + 8) = o1;
-        }
+      for (int q = 0; q < NCH; ++q) {
+        const int d = d0 + 8 * q;
+        if (isv)
+          *reinterpret_cast<uint4*>(pb + key * C::LDV + d * 2) = o[q];
+        else
+          *reinterpret_cast<uint4*>(kb + (d >> 6) * (KT * 128) + swc(key, (d & 63) >> 3)) = o[q];
       }
-      if (tid < 2 * KT) {
-        const int isv = tid >= KT;
-        const int key = isv ? tid - KT : tid;
-        const int sub = key >> 4;
-        const int pos = t * KT + key;
-        const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
-        float sc = live ? 1.f : 0.f;
-        if constexpr (C::DYN)
-          if (live) sc = reinterpret_cast<const float*>(base + C::RAW)[16 * (isv ? SUB + sub : sub) + (key & 15)];
-        (isv ? vsm : ksm)[key] = sc;
+    }
+    if (tid < 2 * KT) {
+      const int isv = tid >= KT;
+      const int key = isv ? tid - KT : tid;
+      const int sub = key >> 4;
+      const int pos = tt * KT + key;
+      const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
+      float sc = live ? 1.f : 0.f;
+      if constexpr (C::DYN)
+        if (live) sc = reinterpret_cast<const float*>(base + C::RAW)[16 * (isv ? SUB + sub : sub) + (key & 15)];
+      (isv ? vsm : ksm)[key] = sc;
+      if constexpr (C::DYN) {
+        // the largest V-scale exponent of the tile's live keys (whole warps)
+        if (isv) {
+          const int e = __reduce_max_sync(0xffffffffu, live ? f32_exp(sc) : -1000);
+          if (lane == 0) etile[(tid - KT) >> 5] = e;
+        }
       }
     }
     __syncthreads();
-    // the raw stage is free: fetch key tile t + NSR into it
-    if (warp == 0 && t + NSR <= t1) {
+    // the raw stage is free: fetch key tile tt + NSR into it
+    if (warp == 0 && tt + NSR <= t1) {
       fence_proxy_async();
-      fetched[st] = issue(t + NSR, st);
+      fetched[st] = issue(tt + NSR, st);
+      pend[st] = tt + NSR;
     }
+    // V^T: rows d, chunks of 8 keys, from the staging copy
+    uint8_t* vb = vt16;
+    for (int u = tid; u < (KT / 8) * (D / 2); u += TWARPS * 32) {
+      const int dp = u % (D / 2), kg = u / (D / 2);
+      uint32_t wv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        wv[k] = *reinterpret_cast<const uint32_t*>(pb + (8 * kg + k) * C::LDV + dp * 4);
+      uint4 e, f;
+      e.x = __byte_perm(wv[0], wv[1], 0x5410);
+      e.y = __byte_perm(wv[2], wv[3], 0x5410);
+      e.z = __byte_perm(wv[4], wv[5], 0x5410);
+      e.w = __byte_perm(wv[6], wv[7], 0x5410);
+      f.x = __byte_perm(wv[0], wv[1], 0x7632);
+      f.y = __byte_perm(wv[2], wv[3], 0x7632);
+      f.z = __byte_perm(wv[4], wv[5], 0x7632);
+      f.w = __byte_perm(wv[6], wv[7], 0x7632);
+      *reinterpret_cast<uint4*>(vb + swc(2 * dp, kg)) = e;
+      *reinterpret_cast<uint4*>(vb + swc(2 * dp + 1, kg)) = f;
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int s2 = 0; s2 < D / 16; ++s2) {
+        const uint64_t da = sw128_desc(q16 + (s2 >> 2) * (TROWS * 128) + (s2 & 3) * 32);
+        const uint64_t db = sw128_desc(kb + (s2 >> 2) * (KT * 128) + (s2 & 3) * 32);
+        umma(tmem, da, db, IDS, s2 > 0);
+      }
+      umma_commit(bar_s);
+    }
+    ++issued_s;
+    return true;
+  };
 
-    // ---- S = Q K^T for this warp's 16 rows and the 64 keys
-    float s[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[j][e] = 0.f;
-    {
-      const int m = lane >> 3;                     // ldmatrix: this lane's matrix
-      const ET* qrow = q16 + (16 * warp + (m & 1) * 8 + (lane & 7)) * LD + (m >> 1) * 8;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t af[4];
-        ldsm_x4(af, qrow + 16 * kk);
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          uint32_t bf[4];
-          ldsm_x4(bf, k16 + (16 * np + (m >> 1) * 8 + (lane & 7)) * LD + 16 * kk + (m & 1) * 8);
-          mma16816<C::BF>(s[2 * np], af, bf[0], bf[1]);
-          mma16816<C::BF>(s[2 * np + 1], af, bf[2], bf[3]);
-        }
+  if (!convert_and_score(t0)) failed = true;
+  for (int t = t0; t <= t1 && !failed; ++t) {
+    // ---- softmax: this warp's half of the row's scores; rescale O; write P'
+    // key tile fully visible to every query row of the CTA: no mask needed
+    const bool fast = have == (1u << SUB) - 1u && t * KT + KT - 1 <= first &&
+                      (a.window <= 0 || t * KT >= pmax + 1 - a.window);
+    const float* kss = ksm;
+    const float* vss = vsm;
+    float sv[KH];
+    // S of this tile, and the last PV (O is rescaled below); warp-uniform, so
+    // the warp-wide tensor-memory loads stay converged
+    bool sok = mbar_wait(bar_s, (uint32_t)((issued_s - 1) & 1));
+    if (issued_o > 0) sok = mbar_wait(bar_o, (uint32_t)((issued_o - 1) & 1)) && sok;
+    sok = __all_sync(0xffffffffu, sok);
+    if (sok) {
+      tc_fence_after();
+      if constexpr (KH == 32) {
+        tmem_ld32(trow + half * KH, sv);
+      } else {
+        tmem_ld16(trow + half * KH, sv);
       }
-    }
-
-    // ---- scores (log2 units) with the causal / window masks of each row
-    float mtA = -INFINITY, mtB = -INFINITY;
-    int et = -1000;
+      float mt = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int key = 8 * j + 2 * lt + c;
-        const int pos = t * KT + key;
-        const float kscale = ksm[key];
-        // a key whose page was not fetched (bad block id) has scale 0: masked
-        const bool okA = pA >= 0 && pos >= loA && pos <= pA && kscale != 0.f;
-        const bool okB = pB >= 0 && pos >= loB && pos <= pB && kscale != 0.f;
-        s[j][c] = okA ? s[j][c] * kscale * fA : -INFINITY;
-        s[j][2 + c] = okB ? s[j][2 + c] * kscale * fB : -INFINITY;
-        mtA = fmaxf(mtA, s[j][c]);
-        mtB = fmaxf(mtB, s[j][2 + c]);
-        if constexpr (C::DYN)
-          if (kscale != 0.f) et = max(et, f32_exp(vsm[key]));
-      }
-#pragma unroll
-    for (int o = 1; o < 4; o <<= 1) {
-      mtA = fmaxf(mtA, __shfl_xor_sync(0xffffffffu, mtA, o));
-      mtB = fmaxf(mtB, __shfl_xor_sync(0xffffffffu, mtB, o));
-    }
-    const float mnA = fmaxf(mA, mtA), mnB = fmaxf(mB, mtB);
-    float alA = (mnA == -INFINITY) ? 1.f : ex2(mA - mnA);
-    float alB = (mnB == -INFINITY) ? 1.f : ex2(mB - mnB);
-    mA = mnA;
-    mB = mnB;
-    lA *= alA;
-    lB *= alB;
-    if constexpr (C::DYN) {
-      // warp-uniform V-scale exponent: every key of the tile is in each quad
-      et = __reduce_max_sync(0xffffffffu, et);
-      const int vnew = max(vexp, max(et, -100));
-      if (vnew != vexp) {
-        const float vfix = pow2i(vexp - vnew);     // 0 on the first data (O is 0)
-        alA *= vfix;
-        alB *= vfix;
-        vexp = vnew;
-        fv = pow2i(PKP - vexp);
-      }
-    }
-    if (__any_sync(0xffffffffu, alA != 1.f || alB != 1.f)) {
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        acc[n][0] *= alA;
-        acc[n][1] *= alA;
-        acc[n][2] *= alB;
-        acc[n][3] *= alB;
-      }
-    }
-    // weights p, row sums, and P' = p x (v_scale 2^(PKP - vexp) | 2^14 | 1)
-    const float muA = (mA == -INFINITY) ? 0.f : mA, muB = (mB == -INFINITY) ? 0.f : mB;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int key = 8 * j + 2 * lt + c;
-        const float pa_ = ex2(s[j][c] - muA), pb_ = ex2(s[j][2 + c] - muB);
-        lA += pa_;
-        lB += pb_;
-        float vf;
-        if constexpr (C::DYN) vf = vsm[key] * fv;
-        else if constexpr (C::BF) vf = 1.f;
-        else vf = 16384.f;
-        s[j][c] = pa_ * vf;
-        s[j][2 + c] = pb_ * vf;
-      }
-
-    // ---- O += P' V: the S accumulators of keys 16kk.. are the A fragments
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t ap[C::NPART][4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int j = 2 * kk + (h >> 1);
-        const int e = (h & 1) * 2;                 // h: 0 (row A, j0) 1 (row B, j0) 2 (A, j1) 3 (B, j1)
-        const float x0 = s[j][e], x1 = s[j][e + 1];
-        if constexpr (C::BF) {
-          const uint32_t h0 = pack_bf16x2(x0, x1);
-          const float r0 = x0 - bf16_lo(h0), r1 = x1 - bf16_lo(h0 >> 16);
-          const uint32_t m0 = pack_bf16x2(r0, r1);
-          ap[0][h] = h0;
-          ap[1][h] = m0;
-          ap[2][h] = pack_bf16x2(r0 - bf16_lo(m0), r1 - bf16_lo(m0 >> 16));
+      for (int j = 0; j < KH; ++j) {
+        const int key = half * KH + j;
+        const float ks = kss[key];
+        if (fast) {
+          sv[j] *= ks;
         } else {
-          const uint32_t h0 = pack_f16x2(x0, x1);
-          ap[0][h] = h0;
-          ap[1][h] = pack_f16x2(x0 - f16_lo(h0), x1 - f16_lo(h0 >> 16));
+          const int pos = t * KT + key;
+          // a key whose page was not fetched (bad block id) has scale 0: masked
+          const bool okj = pA >= 0 && pos >= loA && pos <= pA && ks != 0.f;
+          sv[j] = okj ? sv[j] * ks : -INFINITY;
         }
+        mt = fmaxf(mt, sv[j]);
       }
-      // fragment order: a0 (row g, keys 0-7), a1 (row g+8), a2 (row g, keys 8-15), a3
-      const int m = lane >> 3;
-      const ET* vrow = v16 + (16 * kk + (m & 1) * 8 + (lane & 7)) * LD + (m >> 1) * 8;
-#pragma unroll
-      for (int dn = 0; dn < D / 16; ++dn) {
-        uint32_t bf[4];
-        ldsm_x4_t(bf, vrow + 16 * dn);
-#pragma unroll
-        for (int k = 0; k < C::NPART; ++k) {
-          mma16816<C::BF>(acc[2 * dn], ap[k], bf[0], bf[1]);
-          mma16816<C::BF>(acc[2 * dn + 1], ap[k], bf[2], bf[3]);
-        }
-      }
+      mx[half * TROWS + r] = mt;
     }
-    __syncthreads();                               // K16 / V16 are rewritten next
+    if (__syncthreads_or(!sok)) {
+      failed = true;
+      break;
+    }
+    {
+      // the row's tile max (both halves), in log2 units
+      const float mrow = fmaxf(mx[r], mx[TROWS + r]) * fA;
+      float al = 1.f;
+      if (mrow > mU + TLAZY || (mU == -INFINITY && mrow > -INFINITY)) {
+        al = (mU == -INFINITY) ? 0.f : ex2(mU - mrow);
+        mU = mrow;
+      }
+      // the sum of weights follows the max only; O (whose weights carry the
+      // V-scale factor 2^(TKP - vexp)) also follows the V-scale exponent
+      lH *= al;
+      if constexpr (C::DYN) {
+        // the V-scale exponent is the same for every row (same keys)
+        int et = etile[0];
+        if constexpr (KT > 32) et = max(et, etile[1]);
+        const int vnew = max(vexp, max(et, -100));
+        if (vnew != vexp) {
+          al *= pow2i(vexp - vnew);               // 0 on the first data (O is 0)
+          vexp = vnew;
+          fv = pow2i(TKP - vexp);
+        }
+      }
+      // O holds no data before the first tile's PV; each half rescales its
+      // half of the row's columns
+      if (issued_o > 0 && __any_sync(0xffffffffu, al != 1.f)) {
+#pragma unroll 1
+        for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+          float v[32];
+          tmem_ld32(trow + C::OCOL + c0, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= al;
+          tmem_st32(trow + C::OCOL + c0, v);
+        }
+      }
+      const float mu = (mU == -INFINITY) ? 0.f : mU;
+      uint8_t* pb = p16;
+#pragma unroll
+      for (int c8 = 0; c8 < KH / 8; ++c8) {
+        uint32_t hp[C::NPART][4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          float x[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = 8 * c8 + 2 * e2 + h;
+            const float p = ex2(fmaf(sv[j], fA, -mu));
+            lH += p;
+            float vf;
+            if constexpr (C::DYN) vf = vss[half * KH + j] * fv;
+            else if constexpr (C::BF) vf = 1.f;
+            else vf = TSTATIC;
+            x[h] = p * vf;
+          }
+          if constexpr (C::BF) {
+            const uint32_t h0 = pack_bf16x2(x[0], x[1]);
+            const float r0 = x[0] - bf16_lo(h0), r1 = x[1] - bf16_lo(h0 >> 16);
+            const uint32_t m0 = pack_bf16x2(r0, r1);
+            hp[0][e2] = h0;
+            hp[1][e2] = m0;
+            hp[2 % C::NPART][e2] = pack_bf16x2(r0 - bf16_lo(m0), r1 - bf16_lo(m0 >> 16));
+          } else {
+            const uint32_t h0 = pack_f16x2(x[0], x[1]);
+            hp[0][e2] = h0;
+            hp[1][e2] = pack_f16x2(x[0] - f16_lo(h0), x[1] - f16_hi(h0));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < C::NPART; ++k)
+          *reinterpret_cast<uint4*>(pb + k * C::PB + swc(r, half * (KH / 8) + c8)) =
+              make_uint4(hp[k][0], hp[k][1], hp[k][2], hp[k][3]);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+    }
+    __syncthreads();
+    // ---- O += P' V^T, every term of the split
+    if (tid == 0) {
+      tc_fence_after();
+      const uint8_t* pb = p16;
+      const uint8_t* vb = vt16;
+#pragma unroll
+      for (int k = 0; k < C::NPART; ++k)
+#pragma unroll
+        for (int s2 = 0; s2 < KT / 16; ++s2) {
+          const uint64_t da = sw128_desc(pb + k * C::PB + s2 * 32);
+          const uint64_t db = sw128_desc(vb + s2 * 32);
+          umma(tmem + C::OCOL, da, db, IDO, issued_o > 0 || k > 0 || s2 > 0);
+        }
+      umma_commit(bar_o);
+    }
+    ++issued_o;
+    // the next tile is converted once this PV has read the operands
+    if (t + 1 <= t1 && !convert_and_score(t + 1)) {
+      failed = true;
+      break;
+    }
   }
 
-  // ---- epilogue: out = O x unscale / l per row
-#pragma unroll
-  for (int o = 1; o < 4; o <<= 1) {
-    lA += __shfl_xor_sync(0xffffffffu, lA, o);
-    lB += __shfl_xor_sync(0xffffffffu, lB, o);
-  }
-  float unscale;
-  if constexpr (C::BF) unscale = 1.f;
-  else if constexpr (C::DYN) unscale = pow2i(vexp - PKP);
-  else unscale = vs_static * (1.f / 16384.f);
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int r = half ? rB : rA;
-    const int p = half ? pB : pA;
-    if (p < 0) continue;
-    const float l = half ? lB : lA;
+  // ---- the last PV completes; on a failure, also the last S and every raw
+  // tile still in flight (each wait bounded), so nothing is pending when
+  // tensor memory is freed and the CTA exits
+  bool fin = true;
+  if (issued_o > 0) fin = mbar_wait(bar_o, (uint32_t)((issued_o - 1) & 1));
+  failed = __syncthreads_or(failed || !fin);
+  if (failed) {
+    if (tid == 0) {
+      atomicOr(a.err, ERR_TIMEOUT);
+      if (issued_s > 0) (void)mbar_wait(bar_s, (uint32_t)((issued_s - 1) & 1));
+    }
+    if (warp == 0 && lane == 0)
+      for (int s2 = 0; s2 < NSR; ++s2)
+        if (pend[s2] >= 0) (void)mbar_wait(&bars[s2], (uint32_t)(((pend[s2] - t0) / NSR) & 1));
+  } else {
+    // ---- epilogue: out = O x unscale / l per row; each half stores its half
+    // of the row's columns (the loads are warp-wide; rows without a query
+    // store nothing)
+    mx[half * TROWS + r] = lH;
+    __syncthreads();
+    const float l = mx[r] + mx[TROWS + r];
+    tc_fence_after();
+    float unscale;
+    if constexpr (C::BF) unscale = 1.f;
+    else if constexpr (C::DYN) unscale = pow2i(vexp - TKP);
+    else unscale = vs_static * (1.f / TSTATIC);
     const float f = l > 0.f ? unscale / l : 0.f;
     const int h = r / QP, i = r - h * QP;
     float* dst = a.out + ((long long)(q0 + qt * QP + i) * a.Hq + g * G + h) * D;
+#pragma unroll 1
+    for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+      float v[32];
+      tmem_ld32(trow + C::OCOL + c0, v);
+      if (pA >= 0) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n)
-      *reinterpret_cast<float2*>(dst + 8 * n + 2 * lt) =
-          make_float2(acc[n][2 * half] * f, acc[n][2 * half + 1] * f);
+        for (int i4 = 0; i4 < 8; ++i4)
+          *reinterpret_cast<float4*>(dst + c0 + 4 * i4) =
+              make_float4(v[4 * i4] * f, v[4 * i4 + 1] * f, v[4 * i4 + 2] * f, v[4 * i4 + 3] * f);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(C::TCOLS));
   }
 }
 
 template <int MODE, int D, int G>
-cudaError_t plaunch3(const PrefillArgs& pa, cudaStream_t st) {
-  using C = PCfg<MODE, D>;
+cudaError_t tclaunch3(const PrefillArgs& pa, cudaStream_t st) {
+  using C = TCfg<MODE, D>;
   const DecodeArgs& a = pa.d;
   const long long total = a.num_blocks * a.Hkv * a.bs * (long long)C::RB;
   CUtensorMap km, vm;
@@ -497,7 +726,7 @@ cudaError_t plaunch3(const PrefillArgs& pa, cudaStream_t st) {
   static bool attr_set[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  auto kern = prefill_kernel<MODE, D, G>;
+  auto kern = prefill_tc_kernel<MODE, D, G>;
   if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
@@ -505,34 +734,34 @@ cudaError_t plaunch3(const PrefillArgs& pa, cudaStream_t st) {
   }
   const long long grid = (long long)pa.qtiles * a.B * a.Hkv;
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, PWARPS * 32, C::SMEM, st>>>(pa, km, vm);
+  kern<<<(unsigned)grid, TWARPS * 32, C::SMEM, st>>>(pa, km, vm);
   return cudaGetLastError();
 }
 
 template <int MODE, int D>
-cudaError_t plaunch2(int G, const PrefillArgs& pa, cudaStream_t st) {
+cudaError_t tclaunch2(int G, const PrefillArgs& pa, cudaStream_t st) {
   switch (G) {
-    case 1: return plaunch3<MODE, D, 1>(pa, st);
-    case 2: return plaunch3<MODE, D, 2>(pa, st);
-    case 4: return plaunch3<MODE, D, 4>(pa, st);
-    case 8: return plaunch3<MODE, D, 8>(pa, st);
+    case 1: return tclaunch3<MODE, D, 1>(pa, st);
+    case 2: return tclaunch3<MODE, D, 2>(pa, st);
+    case 4: return tclaunch3<MODE, D, 4>(pa, st);
+    case 8: return tclaunch3<MODE, D, 8>(pa, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int MODE>
-cudaError_t plaunch1(int D, int G, const PrefillArgs& pa, cudaStream_t st) {
+cudaError_t tclaunch1(int D, int G, const PrefillArgs& pa, cudaStream_t st) {
   switch (D) {
-    case 64: return plaunch2<MODE, 64>(G, pa, st);
-    case 128: return plaunch2<MODE, 128>(G, pa, st);
-    case 256: return plaunch2<MODE, 256>(G, pa, st);
+    case 64: return tclaunch2<MODE, 64>(G, pa, st);
+    case 128: return tclaunch2<MODE, 128>(G, pa, st);
+    case 256: return tclaunch2<MODE, 256>(G, pa, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-int prefill_rows_per_cta() { return ROWS; }
+int prefill_rows_per_cta() { return TROWS; }
 
 cudaError_t launch_prefill(int mode, int D, int G, const DecodeArgs& a, const int* query_start,
                            int max_query_len, cudaStream_t st) {
@@ -540,14 +769,14 @@ cudaError_t launch_prefill(int mode, int D, int G, const DecodeArgs& a, const in
   PrefillArgs pa;
   pa.d = a;
   pa.query_start = query_start;
-  const int qp = ROWS / G;
+  const int qp = TROWS / G;
   pa.qtiles = (max_query_len + qp - 1) / qp;
   switch (mode) {
-    case BF16: return plaunch1<BF16>(D, G, pa, st);
-    case FP8_PER_TENSOR: return plaunch1<FP8_PER_TENSOR>(D, G, pa, st);
-    case FP8_PER_HEAD: return plaunch1<FP8_PER_HEAD>(D, G, pa, st);
-    case FP8_PER_TOKEN_HEAD: return plaunch1<FP8_PER_TOKEN_HEAD>(D, G, pa, st);
-    case INT4_PER_TOKEN_HEAD: return plaunch1<INT4_PER_TOKEN_HEAD>(D, G, pa, st);
+    case BF16: return tclaunch1<BF16>(D, G, pa, st);
+    case FP8_PER_TENSOR: return tclaunch1<FP8_PER_TENSOR>(D, G, pa, st);
+    case FP8_PER_HEAD: return tclaunch1<FP8_PER_HEAD>(D, G, pa, st);
+    case FP8_PER_TOKEN_HEAD: return tclaunch1<FP8_PER_TOKEN_HEAD>(D, G, pa, st);
+    case INT4_PER_TOKEN_HEAD: return tclaunch1<INT4_PER_TOKEN_HEAD>(D, G, pa, st);
     default: return cudaErrorInvalidValue;
   }
 }
