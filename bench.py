@@ -515,7 +515,8 @@ def run_gpu(args):
     fill_ms, fill_T, fill_mode = st["fill"]
     wb_fill = write_bytes(w, fill_mode, fill_T)
     fill_gbs = wb_fill / (fill_ms * 1e-3) / 1e9
-    traffic = profiled_traffic("decode.cu", f"decode_{args.workload}_{args.mode}.md")
+    summary = f"decode_{args.workload}_{args.mode}.md"
+    traffic = profiled_traffic("decode.cu", summary)
     mode_name = args.mode + ("+bf16_sliding" if args.skip_sliding else "")
     res = {
         "metric": METRIC,
@@ -546,7 +547,10 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
                      "kernel": "decode_kernel (+ log-sum-exp merge)",
-                     "peak_source": f"{peak_src} hbm_gbs"},
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "traffic_source": (f"profiles/{summary}: ncu dram bytes per launch, "
+                                        "captured on the same decode.cu (sha256 checked), "
+                                        "not measured in this run") if traffic else None},
         "e2e": {"value": round(all_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
