@@ -56,6 +56,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return true;
 }
 
+// True in exactly one active lane of the warp (elect.sync).  Copies issued
+// under it take their operands from that lane alone, without the per-lane
+// loop a branch on the lane index needs.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{ .reg .b32 rx; .reg .pred px; elect.sync rx|px, 0xffffffff; selp.b32 %0, 1, 0, px; }"
+               : "=r"(pred));
+  return pred != 0;
+}
+
 // Global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte
 // aligned) completing on `bar`.
 __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,

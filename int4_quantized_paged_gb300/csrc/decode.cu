@@ -551,7 +551,8 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     pst = (pst + 1 == NS) ? 0 : pst + 1;
     const int pos0 = (p.t0 + p.k) * TILE;
     if (blk >= 0 && blk < a.num_blocks) {
-      if (lane == 0) {
+      // every lane holds the same block id and cursor: any one lane issues
+      if (elect_one()) {
         const unsigned cell = ((unsigned)blk * (unsigned)a.Hkv + (unsigned)p.g) * (unsigned)a.bs +
                               (unsigned)(pos0 & (a.bs - 1));
         const int row = (int)(((unsigned long long)cell * C::RB) >> 7);
