@@ -996,7 +996,9 @@ def run_prefill(args):
                        "tokens_per_s": round(T / (ms * 1e-3), 1)},
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
-                         "kernel": "prefill_kernel (mma.sync f16, P split in two terms)",
+                         "kernel": ("prefill_ws_kernel (tcgen05, warp-specialised, P' f16 hi + lo "
+                                    "in tensor memory)" if mode != kvq.BF16 and w.D in (64, 128)
+                                    else "prefill_tc_kernel (tcgen05, P' split in shared memory)"),
                          "peak_source": f"{src} bf16 dense"},
             "gpu_launches": n, "clocks": clocks}
 

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "libkvq.so")
 BUILD = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "write.cu", "decode.cu", "prefill.cu"]
+SOURCES = ["api.cu", "write.cu", "decode.cu", "prefill.cu", "prefill_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -71,6 +71,10 @@ bool decode_supported(int mode, int D, int G);
 // caches, scales, block table, context lengths, q and out (no workspace).
 cudaError_t launch_prefill(int mode, int D, int G, const DecodeArgs& a, const int* query_start,
                            int max_query_len, cudaStream_t st);
+// Warp-specialised prefill for quantized layers of head_dim 64 or 128.
+bool prefill_ws_supports(int mode, int D);
+cudaError_t launch_prefill_ws(int mode, int D, int G, const DecodeArgs& a, const int* query_start,
+                              int max_query_len, cudaStream_t st);
 int prefill_rows_per_cta();
 // Resident decode CTAs per SM on the current device (0 if unknown: no device).
 int decode_ctas_per_sm(int mode, int D, int G);

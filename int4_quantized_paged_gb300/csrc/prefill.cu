@@ -50,6 +50,8 @@
 
 #include "async_copy.cuh"
 #include "kvq_internal.h"
+#include "prefill_common.cuh"
+#include "tcgen05.cuh"
 #include "tile_math.cuh"
 
 namespace kvq {
@@ -60,106 +62,6 @@ constexpr int TROWS = 128;                 // query rows per CTA (the MMA's M)
 constexpr int TKP = 6;                     // P' = p v_scale 2^(TKP - vexp) < 2^15 (p <= 2^8)
 constexpr float TLAZY = 8.f;               // the row's reference max moves when exceeded by this
 constexpr float TSTATIC = 64.f;            // P' = p x 64 for static FP8 scales (< 2^14)
-
-// ------------------------------------------------------------ tcgen05 wrappers
-// Shared-memory matrix descriptor of a K-major operand in the canonical
-// 128-byte-swizzle layout: rows of 128 bytes (64 f16 of K), 8-row groups 1024
-// bytes apart, 16-byte chunk c of row r stored at chunk c ^ (r & 7).  The
-// start address may be advanced by 32-byte steps along K inside a row.
-__device__ __forceinline__ uint64_t sw128_desc(const void* p) {
-  const uint32_t a = smem_u32(p);
-  uint64_t d = (uint64_t)((a >> 4) & 0x3FFFu);      // start address / 16
-  d |= (uint64_t)1 << 16;                            // leading offset (unused here)
-  d |= (uint64_t)(1024 >> 4) << 32;                  // stride between 8-row groups
-  d |= (uint64_t)1 << 46;                            // descriptor version
-  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor: f32 accumulator, f16 (BF false) or bf16 operands,
-// both K-major, M x N.
-template <bool BF>
-__host__ __device__ constexpr uint32_t mma_idesc(int M, int N) {
-  return (1u << 4) | ((BF ? 1u : 0u) << 7) | ((BF ? 1u : 0u) << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
-                                     bool accumulate) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
-      "l"(da), "l"(db), "r"(idesc), "r"((uint32_t)accumulate));
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// Byte offset of 16-byte chunk `c` of row `r` in a 128-byte-swizzled block.
-__device__ __forceinline__ uint32_t swc(int r, int c) {
-  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
-}
 
 // ------------------------------------------------------------ configuration
 template <int MODE, int D>
@@ -195,44 +97,6 @@ struct TCfg {
   static constexpr int OCOL = KT;                           // S: [0, KT), O: [KT, KT + D)
   static constexpr int TCOLS = (OCOL + D <= 128) ? 128 : ((OCOL + D <= 256) ? 256 : 512);
 };
-
-struct PrefillArgs {
-  DecodeArgs d;                  // caches, scales, block table, context_lens, q, out
-  const int* query_start;        // [B + 1]
-  int qtiles;                    // query tiles per (sequence, KV head) in the grid
-};
-
-// 16 raw code bytes -> their f16 (bf16 for BF16) values: 8 (BF16), 16 (FP8)
-// or 32 (INT4) elements, as 1, 2 or 4 16-byte chunks.  Exact.
-template <int MODE>
-__device__ __forceinline__ void convert16(uint4 w, uint4 (&o)[4]) {
-  if constexpr (MODE == BF16) {
-    o[0] = w;
-  } else if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t x = ws[q];
-      // low nibble of byte j = element 2j: e = {b0.lo, b1.lo}, h = 16 {b0.hi, b1.hi}
-      const uint32_t e0 = nib2_f16x2<0>(__byte_perm(x, 0u, 0x7170));
-      const uint32_t h0 = nib2_f16x2<1>(__byte_perm(x, 0u, 0x7170));
-      const uint32_t e1 = nib2_f16x2<0>(__byte_perm(x, 0u, 0x7372));
-      const uint32_t h1 = nib2_f16x2<1>(__byte_perm(x, 0u, 0x7372));
-      uint32_t hs0, hs1;
-      asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hs0) : "r"(h0), "r"(0x2C002C00u));   // x 1/16
-      asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hs1) : "r"(h1), "r"(0x2C002C00u));
-      o[q].x = __byte_perm(e0, hs0, 0x5410);
-      o[q].y = __byte_perm(e0, hs0, 0x7632);
-      o[q].z = __byte_perm(e1, hs1, 0x5410);
-      o[q].w = __byte_perm(e1, hs1, 0x7632);
-    }
-  } else {
-    e4m3x4_f16(w.x, o[0].x, o[0].y);
-    e4m3x4_f16(w.y, o[0].z, o[0].w);
-    e4m3x4_f16(w.z, o[1].x, o[1].y);
-    e4m3x4_f16(w.w, o[1].z, o[1].w);
-  }
-}
 
 template <int MODE, int D, int G>
 __global__ void __launch_bounds__(TWARPS * 32, 1)
@@ -766,6 +630,8 @@ int prefill_rows_per_cta() { return TROWS; }
 cudaError_t launch_prefill(int mode, int D, int G, const DecodeArgs& a, const int* query_start,
                            int max_query_len, cudaStream_t st) {
   if (a.B == 0 || max_query_len <= 0) return cudaSuccess;
+  if (prefill_ws_supports(mode, D))
+    return launch_prefill_ws(mode, D, G, a, query_start, max_query_len, st);
   PrefillArgs pa;
   pa.d = a;
   pa.query_start = query_start;

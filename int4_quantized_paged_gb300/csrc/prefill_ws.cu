@@ -1,0 +1,651 @@
+// Prefill (chunked multi-query) attention over a quantized paged cache (FP8 or
+// INT4 codes, head_dim 64 or 128), warp-specialised on the fifth-generation
+// tensor cores.  It computes what the single-role prefill kernel computes
+// (causal attention of each new token's query over the retained positions,
+// the scales folded into score and weight: "Per-tensor vs per-head FP8 KV
+// cache scales", section "Use a three-stage decision"; "FP8 KV cache layer
+// skipping vs per-head scales", section "Run a four-way ablation") with the
+// work of one key tile spread over warps with their own roles, so that the
+// tensor cores, the code conversion and the softmax run at the same time.
+//
+// A CTA owns two query tiles of M = 128 rows each (128/G consecutive new
+// positions times the G query heads of one KV head; tile 1 follows tile 0),
+// and streams the keys of both in tiles of 64 positions.  Roles (14 warps):
+//  * warp 12, producer: 2-D TMA copies of the key tile's K and V page tiles
+//    (and 64-byte bulk copies of their dynamic scales) into a ring of raw
+//    stages; lane s takes page tile s.
+//  * warps 8-11, converters: raw codes -> f16 in the tensor cores' layout,
+//    K as 64 rows of D (K-major, 128-byte swizzle) and V transposed (D rows
+//    of 64 keys) through a row-major staging copy; K and V scales (zero for a
+//    key outside the CTA's range or on a page that was not fetched) and the
+//    tile's largest V-scale exponent.  Two operand buffers.
+//  * warp 13, MMA issuer (one thread): S_j = Q_j K^T (M 128, N 64) into
+//    tensor memory for each query tile j, and O_j += P'_j V with P'_j read
+//    from tensor memory, every term of its f16 hi + lo split.  Order per key
+//    tile t: PV_0(t), S_0(t+1), PV_1(t), S_1(t+1), so that the tensor cores
+//    work on one query tile while the softmax of the other runs.
+//  * warps 0-3 and 4-7, softmax of query tile 0 and 1: one thread per row
+//    (its tensor-memory lane) loads the row's 64 scores, applies the K scale
+//    and masks, keeps a lazily moved reference max (moved only when a tile
+//    exceeds it by more than 2^8), rescales the row of O in tensor memory
+//    when it moves, and stores P' = p x v_scale x 2^k (f16 hi + lo) into the
+//    query tile's own P' columns of tensor memory.
+// Tensor memory: S_0, S_1, P'_0, P'_1 (64 columns each), O_0, O_1 (D each).
+// Every wait is bounded; a wait that runs out flags TIMEOUT and sets a
+// shared abort flag that ends every role's loop, the work already issued is
+// waited for (bounded again), and tensor memory is freed before the CTA exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "async_copy.cuh"
+#include "kvq_internal.h"
+#include "prefill_common.cuh"
+#include "tcgen05.cuh"
+#include "tile_math.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int WS_SOFT = 8;                          // softmax warps (two warpgroups)
+constexpr int WS_CONV = 4;                          // converter warps
+constexpr int WS_PROD = WS_SOFT + WS_CONV;          // producer warp
+constexpr int WS_MMA = WS_PROD + 1;                 // MMA-issuing warp
+constexpr int WS_THREADS = (WS_MMA + 1) * 32;       // 448
+constexpr int WROWS = 128;                          // rows per query tile (the MMA's M)
+constexpr int WKT = 64;                             // keys per tile
+constexpr int WKP = 6;                              // P' = p v_scale 2^(WKP - vexp) < 2^15 (p <= 2^8)
+constexpr float WLAZY = 8.f;                        // the reference max moves when exceeded by this
+constexpr float WSTATIC = 64.f;                     // P' = p x 64 for static FP8 scales (< 2^14)
+constexpr int CONV_BAR = 1;                         // named barrier of the converter warps
+
+template <int MODE, int D>
+struct WCfg {
+  static constexpr int RB = row_bytes<MODE>(D);
+  static constexpr int TB = 16 * RB;                       // one page tile (16 positions)
+  static constexpr int TBP = (TB + 1023) / 1024 * 1024;
+  static constexpr bool DYN = (MODE == FP8_PER_TOKEN_HEAD || MODE == INT4_PER_TOKEN_HEAD);
+  static constexpr int SUB = WKT / 16;                      // page tiles per key tile
+  static constexpr int RAW = 2 * SUB * TBP;                 // K and V page tiles of a key tile
+  static constexpr int SCB = DYN ? 2 * SUB * 64 : 0;        // their K and V scales
+  static constexpr int RAWS = (RAW + SCB + 1023) / 1024 * 1024;
+  static constexpr int QB = WROWS * D * 2;                  // one query tile: D/64 blocks of 128 x 128 B
+  static constexpr int KB = WKT * D * 2;                    // one K buffer: D/64 blocks of 64 x 128 B
+  static constexpr int VTB = D * WKT * 2;                   // one V^T buffer: D rows of 128 B
+  static constexpr int LDV = (D + 8) * 2;                   // row pitch of the V staging copy
+  static constexpr int STG = (WKT * LDV + 1023) / 1024 * 1024;
+  // one scale buffer: K scales, V scales, then ints: V-scale exponent of
+  // each 32-key half, whether every page tile was fetched
+  static constexpr int SCS = 2 * WKT * 4 + 16;
+  static constexpr int ROWB = 2 * 2 * WROWS * 4;            // row factor and position per row
+  static constexpr int BARB = 32 * 8;                       // barriers
+  static constexpr int FIXED = 2 * QB + 2 * KB + 2 * VTB + STG + 2 * SCS + ROWB + BARB + 64;
+  static constexpr int LIMIT = 232448 - 1024;               // per-CTA shared memory, minus slack
+  static constexpr int NR = (FIXED + 4 * RAWS <= LIMIT) ? 4 : ((FIXED + 3 * RAWS <= LIMIT) ? 3 : 2);
+  static constexpr int SMEM = NR * RAWS + FIXED + 1024;
+  // tensor-memory columns
+  static constexpr int SCOL = 0;                            // S_j at 64 j
+  static constexpr int PCOL = 128;                          // P'_j at 128 + 64 j (hi 32, lo 32)
+  static constexpr int OCOL = 256;                          // O_j at 256 + D j
+  static constexpr int TCOLS = 512;
+  static_assert(OCOL + 2 * D <= TCOLS, "tensor memory");
+  static_assert(SMEM <= 232448, "shared memory");
+};
+
+template <int MODE, int D, int G>
+__global__ void __launch_bounds__(WS_THREADS, 1)
+    prefill_ws_kernel(const PrefillArgs pa, const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap) {
+  using C = WCfg<MODE, D>;
+  const DecodeArgs& a = pa.d;
+  constexpr int SUB = C::SUB;
+  constexpr int NR = C::NR;
+  constexpr int QP = WROWS / G;                // positions per query tile
+  constexpr int CPR = C::RB / 16;              // 16-byte raw chunks per position row
+  constexpr int EPC = (MODE == INT4_PER_TOKEN_HEAD) ? 32 : 16;   // elements per raw chunk
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* raw = smem;                                       // NR stages
+  uint8_t* q16 = raw + NR * C::RAWS;                         // 2 query tiles
+  uint8_t* k16 = q16 + 2 * C::QB;                            // 2 K buffers
+  uint8_t* vt16 = k16 + 2 * C::KB;                           // 2 V^T buffers
+  uint8_t* stg = vt16 + 2 * C::VTB;                          // V staging copy
+  uint8_t* scb = stg + C::STG;                               // 2 scale buffers
+  float* rowf = reinterpret_cast<float*>(scb + 2 * C::SCS);  // [2][128] score factor per row
+  int* rowp = reinterpret_cast<int*>(rowf + 2 * WROWS);      // [2][128] position (-1: no row)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rowp + 2 * WROWS);
+  uint64_t* raw_full = bars;                                 // [NR] producer -> converters
+  uint64_t* raw_empty = raw_full + NR;                       // [NR] converters -> producer
+  uint64_t* kv_full = raw_empty + NR;                        // [2] converters -> MMA
+  uint64_t* kv_empty = kv_full + 2;                          // [2] MMA (commit) -> converters
+  uint64_t* s_full = kv_empty + 2;                           // [2] MMA (commit) -> softmax j
+  uint64_t* p_full = s_full + 2;                             // [2] softmax j (128 arrivals) -> MMA
+  uint64_t* o_fin = p_full + 2;                              // MMA (commit) -> softmax, at the end
+  int* s_have = reinterpret_cast<int*>(bars + 32);           // [NR] fetched page tiles per stage
+  volatile int* s_abort = s_have + 4;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_have + 5);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- this CTA's (sequence, KV head, pair of query tiles); latest first
+  const int per_tile = a.B * a.Hkv;
+  const int ct = pa.qtiles - 1 - (int)(blockIdx.x / per_tile);
+  const int rem = (int)(blockIdx.x % per_tile);
+  const int b = rem / a.Hkv, g = rem - b * a.Hkv;
+  const int q0 = pa.query_start[b];
+  const int n_b = pa.query_start[b + 1] - q0;
+  const int L = a.context_lens[b];
+  if (ct * 2 * QP >= n_b || n_b <= 0) return;               // whole CTA: before any barrier
+  if (L < n_b || (long long)L > ((long long)a.max_blocks << a.bs_shift)) {
+    if (tid == 0) atomicOr(a.err, ERR_BAD_INDEX);
+    return;
+  }
+  const int qbase = ct * 2 * QP;                            // query index of tile 0, row 0
+  const int first = L - n_b + qbase;                        // its position
+  const int nq = min(2 * QP, n_b - qbase);                  // valid query positions here
+  const int pmax = first + nq - 1;
+  const int kmin = (a.window > 0) ? max(0, first + 1 - a.window) : 0;
+  const int t0 = kmin / WKT, t1 = pmax / WKT;               // key tiles, inclusive
+  const int ntl = t1 - t0 + 1;
+
+  if (tid == 0) {
+    for (int s = 0; s < NR; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 4 * 32);
+    }
+    mbar_init(o_fin, 1);
+    mbar_init_fence();
+    *s_abort = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(s_tmem)),
+                 "r"(C::TCOLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+
+  // ---- queries of both tiles: row R = 128 j + h * QP + i -> query index
+  // qbase + j * QP + i, head g*G + h, prescaled by a power of two so the bf16
+  // values are exact in f16.  Lane l holds elements l + 32e of the row.
+  float ks_static = 1.f;
+  if constexpr (MODE == FP8_PER_TENSOR) ks_static = a.k_scale[0];
+  if constexpr (MODE == FP8_PER_HEAD) ks_static = a.k_scale[g];
+  for (int R = warp; R < 2 * WROWS; R += WS_THREADS / 32) {
+    const int j = R / WROWS, r = R - j * WROWS;
+    const int h = r / QP, i = r - h * QP;
+    const int qi = j * QP + i;                               // query index within the CTA
+    const bool valid = qi < nq;
+    constexpr int EL = D / 32;
+    float x[EL];
+    float amax = 0.f;
+    if (valid) {
+      const uint16_t* src = a.q + ((long long)(q0 + qbase + qi) * a.Hq + g * G + h) * D;
+#pragma unroll
+      for (int e = 0; e < EL; ++e) {
+        x[e] = __uint_as_float((uint32_t)src[lane + 32 * e] << 16);
+        amax = fmaxf(amax, fabsf(x[e]));
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < EL; ++e) x[e] = 0.f;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int qexp = 0;
+    if (amax > 0.f) qexp = max(((int)(__float_as_uint(amax) >> 23) & 0xFF) - 127, -100);
+    const float qmul = pow2i(14 - qexp);
+    uint8_t* qt = q16 + j * C::QB;
+#pragma unroll
+    for (int e = 0; e < EL; ++e) {
+      const int d = lane + 32 * e;
+      const uint16_t h16 = (uint16_t)(pack_f16x2(x[e] * qmul, 0.f) & 0xFFFFu);
+      *reinterpret_cast<uint16_t*>(qt + (d >> 6) * (WROWS * 128) + swc(r, (d & 63) >> 3) + (d & 7) * 2) = h16;
+    }
+    if (lane == 0) {
+      rowf[R] = a.qk_scale * ks_static * pow2i(qexp - 14);
+      rowp[R] = valid ? first + qi : -1;
+    }
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  // ================================================================ roles
+  if (warp == WS_PROD) {
+    // ---- producer: key tile t into raw stage (t - t0) % NR; lane s < SUB
+    // copies page tile s.  Page tiles wholly outside [kmin, pmax] are not
+    // fetched.
+    int last[NR];                                  // tile index last issued into each stage
+#pragma unroll
+    for (int s = 0; s < NR; ++s) last[s] = -1;
+    for (int i = 0; i < ntl; ++i) {
+      const int st = i % NR;
+      if (i >= NR) {
+        const bool ok = mbar_wait(&raw_empty[st], (uint32_t)((i / NR - 1) & 1));
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
+          break;
+        }
+      }
+      if (__any_sync(0xffffffffu, *s_abort)) break;
+      const int t = t0 + i;
+      const int pos = t * WKT + 16 * lane;
+      int blk = -1;
+      bool want = false;
+      if (lane < SUB) {
+        want = pos + 16 > kmin && pos <= pmax;
+        if (want) {
+          blk = __ldg(a.block_table + (long long)b * a.max_blocks + (pos >> a.bs_shift));
+          if (blk < 0 || blk >= a.num_blocks) {
+            atomicOr(a.err, ERR_BAD_INDEX);
+            want = false;
+          }
+        }
+      }
+      const unsigned fetch = __ballot_sync(0xffffffffu, want);
+      uint8_t* base = raw + st * C::RAWS;
+      fence_proxy_async();
+      if (lane == 0) {
+        s_have[st] = (int)fetch;
+        mbar_expect_tx(&raw_full[st], (uint32_t)__popc(fetch) * (2 * C::TB + (C::DYN ? 128 : 0)));
+      }
+      __syncwarp();
+      if (want) {
+        const unsigned cell = ((unsigned)blk * (unsigned)a.Hkv + (unsigned)g) * (unsigned)a.bs +
+                              (unsigned)(pos & (a.bs - 1));
+        const int rowc = (int)(((unsigned long long)cell * C::RB) >> 7);
+        tma_tile_2d(base + lane * C::TBP, &kmap, 0, rowc, &raw_full[st]);
+        tma_tile_2d(base + (SUB + lane) * C::TBP, &vmap, 0, rowc, &raw_full[st]);
+        if constexpr (C::DYN) {
+          float* sc = reinterpret_cast<float*>(base + C::RAW);
+          bulk_copy(sc + 16 * lane, a.k_cs + cell, 64, &raw_full[st]);
+          bulk_copy(sc + 16 * (SUB + lane), a.v_cs + cell, 64, &raw_full[st]);
+        }
+      }
+      last[st] = i;
+    }
+    // every copy issued has landed before the CTA exits (bounded waits)
+    if (lane == 0)
+#pragma unroll
+      for (int s = 0; s < NR; ++s)
+        if (last[s] >= 0) (void)mbar_wait(&raw_full[s], (uint32_t)((last[s] / NR) & 1));
+  } else if (warp >= WS_SOFT && warp < WS_PROD) {
+    // ---- converters (128 threads)
+    const int ct_ = tid - WS_SOFT * 32;
+    for (int i = 0; i < ntl; ++i) {
+      const int st = i % NR, buf = i & 1;
+      const int t = t0 + i;
+      bool ok = mbar_wait(&raw_full[st], (uint32_t)((i / NR) & 1));
+      if (i >= 2) ok = mbar_wait(&kv_empty[buf], (uint32_t)((i / 2 - 1) & 1)) && ok;
+      if (!ok) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
+      // every converter thread takes the same decision (a barrier reduction)
+      if (named_sync_or(CONV_BAR, WS_CONV * 32, !ok || *s_abort)) break;
+      const unsigned have = (unsigned)s_have[st];
+      const uint8_t* base = raw + st * C::RAWS;
+      uint8_t* kb = k16 + buf * C::KB;
+      // K into kb, V into the row-major staging copy (zeros where nothing was
+      // fetched or the position lies outside [kmin, pmax])
+      for (int c = ct_; c < 2 * WKT * CPR; c += WS_CONV * 32) {
+        const int isv = c >= WKT * CPR;
+        const int cc = isv ? c - WKT * CPR : c;
+        const int key = cc / CPR, ch = cc - key * CPR;
+        const int sub = key >> 4, kr = key & 15;
+        const int pos = t * WKT + key;
+        const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (live)
+          w = *reinterpret_cast<const uint4*>(base + (isv ? SUB + sub : sub) * C::TBP +
+                                             swz((uint32_t)(kr * C::RB + ch * 16)));
+        uint4 o[4];
+        convert16<MODE>(w, o);
+        constexpr int NCH = EPC / 8;
+        const int d0 = ch * EPC;
+#pragma unroll
+        for (int qq = 0; qq < NCH; ++qq) {
+          const int d = d0 + 8 * qq;
+          if (isv)
+            *reinterpret_cast<uint4*>(stg + key * C::LDV + d * 2) = o[qq];
+          else
+            *reinterpret_cast<uint4*>(kb + (d >> 6) * (WKT * 128) + swc(key, (d & 63) >> 3)) = o[qq];
+        }
+      }
+      {
+        // scales: threads 0..63 K, 64..127 V (scale 0: no key)
+        float* ksm = reinterpret_cast<float*>(scb + buf * C::SCS);
+        float* vsm = ksm + WKT;
+        int* tinfo = reinterpret_cast<int*>(vsm + WKT);
+        const int isv = ct_ >= WKT;
+        const int key = isv ? ct_ - WKT : ct_;
+        const int sub = key >> 4;
+        const int pos = t * WKT + key;
+        const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
+        float sc = live ? 1.f : 0.f;
+        if constexpr (C::DYN)
+          if (live) sc = reinterpret_cast<const float*>(base + C::RAW)[16 * (isv ? SUB + sub : sub) + (key & 15)];
+        (isv ? vsm : ksm)[key] = sc;
+        if constexpr (C::DYN) {
+          if (isv) {
+            const int e = __reduce_max_sync(0xffffffffu, live ? f32_exp(sc) : -1000);
+            if (lane == 0) tinfo[(ct_ - WKT) >> 5] = e;
+          }
+        }
+        if (ct_ == 0) tinfo[2] = (have == (1u << SUB) - 1u) ? 1 : 0;
+      }
+      named_sync(CONV_BAR, WS_CONV * 32);
+      // the raw stage has been read
+      if (ct_ == 0) mbar_arrive(&raw_empty[st]);
+      // V^T: rows d, chunks of 8 keys, from the staging copy
+      uint8_t* vb = vt16 + buf * C::VTB;
+      for (int u = ct_; u < (WKT / 8) * (D / 2); u += WS_CONV * 32) {
+        const int dp = u % (D / 2), kg = u / (D / 2);
+        uint32_t wv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          wv[k] = *reinterpret_cast<const uint32_t*>(stg + (8 * kg + k) * C::LDV + dp * 4);
+        uint4 e, f;
+        e.x = __byte_perm(wv[0], wv[1], 0x5410);
+        e.y = __byte_perm(wv[2], wv[3], 0x5410);
+        e.z = __byte_perm(wv[4], wv[5], 0x5410);
+        e.w = __byte_perm(wv[6], wv[7], 0x5410);
+        f.x = __byte_perm(wv[0], wv[1], 0x7632);
+        f.y = __byte_perm(wv[2], wv[3], 0x7632);
+        f.z = __byte_perm(wv[4], wv[5], 0x7632);
+        f.w = __byte_perm(wv[6], wv[7], 0x7632);
+        *reinterpret_cast<uint4*>(vb + swc(2 * dp, kg)) = e;
+        *reinterpret_cast<uint4*>(vb + swc(2 * dp + 1, kg)) = f;
+      }
+      fence_proxy_async();
+      named_sync(CONV_BAR, WS_CONV * 32);
+      if (ct_ == 0) mbar_arrive(&kv_full[buf]);
+    }
+  } else if (warp == WS_MMA) {
+    // ---- MMA issuer: lane 0 issues and commits; the warp waits together
+    constexpr uint32_t IDS = mma_idesc<false>(WROWS, WKT);
+    constexpr uint32_t IDO = mma_idesc<false>(WROWS, D);
+    auto wait = [&](uint64_t* bar, uint32_t par) -> bool {
+      const bool w = __all_sync(0xffffffffu, mbar_wait(bar, par));
+      if (!w && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
+      return w && !__any_sync(0xffffffffu, *s_abort);
+    };
+    // S_j = Q_j K^T from K buffer kbuf
+    auto issue_s = [&](int j, int kbuf) {
+      if (lane == 0) {
+        tc_fence_after();
+        const uint8_t* qa = q16 + j * C::QB;
+        const uint8_t* kb = k16 + kbuf * C::KB;
+#pragma unroll
+        for (int s2 = 0; s2 < D / 16; ++s2) {
+          const uint64_t da = sw128_desc(qa + (s2 >> 2) * (WROWS * 128) + (s2 & 3) * 32);
+          const uint64_t db = sw128_desc(kb + (s2 >> 2) * (WKT * 128) + (s2 & 3) * 32);
+          umma(tmem + C::SCOL + 64 * j, da, db, IDS, s2 > 0);
+        }
+        umma_commit(&s_full[j]);
+      }
+      __syncwarp();
+    };
+    // O_j += P'_j V, both terms of the split, V^T from buffer vbuf
+    auto issue_pv = [&](int j, int vbuf, bool acc) {
+      if (lane == 0) {
+        tc_fence_after();
+        const uint8_t* vb = vt16 + vbuf * C::VTB;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int kk = 0; kk < WKT / 16; ++kk)
+            umma_tmem_a(tmem + C::OCOL + D * j, tmem + C::PCOL + 64 * j + 32 * h + 8 * kk,
+                        sw128_desc(vb + kk * 32), IDO, acc || h > 0 || kk > 0);
+      }
+      __syncwarp();
+    };
+    if (wait(&kv_full[0], 0u)) {
+      issue_s(0, 0);
+      issue_s(1, 0);
+      for (int i = 0; i < ntl; ++i) {
+        const int buf = i & 1;
+        const bool more = i + 1 < ntl;
+        if (!wait(&p_full[0], (uint32_t)(i & 1))) break;
+        issue_pv(0, buf, i > 0);
+        if (more) {
+          if (!wait(&kv_full[buf ^ 1], (uint32_t)(((i + 1) >> 1) & 1))) break;
+          issue_s(0, buf ^ 1);
+        }
+        if (!wait(&p_full[1], (uint32_t)(i & 1))) break;
+        issue_pv(1, buf, i > 0);
+        // both PVs of this key tile have read its operands: buffer free
+        if (lane == 0) umma_commit(&kv_empty[buf]);
+        __syncwarp();
+        if (more) issue_s(1, buf ^ 1);
+      }
+    }
+    // everything issued completes before the epilogue and the exit
+    if (lane == 0) umma_commit(o_fin);
+    __syncwarp();
+    (void)mbar_wait(o_fin, 0u);
+  } else {
+    // ---- softmax of query tile j: one thread per row (its tensor-memory lane)
+    const int j = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const int R = j * WROWS + r;
+    const int pA = rowp[R];
+    const int loA = (a.window > 0) ? max(0, pA + 1 - a.window) : 0;
+    const float fA = rowf[R];
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t tS = trow + C::SCOL + 64 * j;
+    const uint32_t tP = trow + C::PCOL + 64 * j;
+    const uint32_t tO = trow + C::OCOL + D * j;
+    // positions of this query tile's first and last rows: a key tile inside
+    // [last row's window start, first row] is visible to every row
+    const int firstj = first + j * QP;
+    const int pmaxj = min(firstj + QP - 1, pmax);
+    // mU: the row's reference max (log2 units) the weights are taken against;
+    // it moves only when a tile exceeds it by more than WLAZY, so O is
+    // rescaled rarely and the weights stay below 2^WLAZY
+    float mU = -INFINITY, l = 0.f;
+    int vexp = -1000;
+    float fv = 0.f;                                  // 2^(WKP - vexp)
+    float vs_static = 1.f;
+    if constexpr (MODE == FP8_PER_TENSOR) vs_static = a.v_scale[0];
+    if constexpr (MODE == FP8_PER_HEAD) vs_static = a.v_scale[g];
+    bool ok = true;
+    for (int i = 0; i < ntl; ++i) {
+      const int buf = i & 1, t = t0 + i;
+      const bool w = __all_sync(0xffffffffu, mbar_wait(&s_full[j], (uint32_t)(i & 1)));
+      if (!w && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
+      if (!w || __any_sync(0xffffffffu, *s_abort)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t s0[32], s1[32];
+      tmem_ld32_nowait(tS, s0);
+      tmem_ld32_nowait(tS + 32, s1);
+      tmem_wait_ld();
+      const float* ksm = reinterpret_cast<const float*>(scb + buf * C::SCS);
+      const float* vsm = ksm + WKT;
+      const int* tinfo = reinterpret_cast<const int*>(vsm + WKT);
+      const bool fast = tinfo[2] != 0 && t * WKT + WKT - 1 <= firstj &&
+                        (a.window <= 0 || t * WKT >= pmaxj + 1 - a.window);
+      float sv[WKT];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < WKT; ++k) {
+        const float ks = ksm[k];
+        float x = __uint_as_float(k < 32 ? s0[k] : s1[k - 32]);
+        if (fast) {
+          x *= ks;
+        } else {
+          const int pos = t * WKT + k;
+          // a key outside the CTA's range or on a page not fetched has scale 0
+          const bool okk = pA >= 0 && pos >= loA && pos <= pA && ks != 0.f;
+          x = okk ? x * ks : -INFINITY;
+        }
+        sv[k] = x;
+        mt = fmaxf(mt, x);
+      }
+      const float mrow = mt * fA;
+      float al = 1.f;
+      if (mrow > mU + WLAZY || (mU == -INFINITY && mrow > -INFINITY)) {
+        al = (mU == -INFINITY) ? 0.f : ex2(mU - mrow);
+        mU = mrow;
+      }
+      // the sum of weights follows the max only; O (whose weights carry the
+      // V-scale factor 2^(WKP - vexp)) also follows the V-scale exponent
+      l *= al;
+      if constexpr (C::DYN) {
+        const int et = max(tinfo[0], tinfo[1]);     // the same for every row (same keys)
+        const int vnew = max(vexp, max(et, -100));
+        if (vnew != vexp) {
+          al *= pow2i(vexp - vnew);                 // 0 on the first data (O is 0)
+          vexp = vnew;
+          fv = pow2i(WKP - vexp);
+        }
+      }
+      // O holds data from the first PV on (its completion precedes S of this tile)
+      if (i > 0 && __any_sync(0xffffffffu, al != 1.f)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float v[32];
+          tmem_ld32(tO + c0, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] *= al;
+          tmem_st32(tO + c0, v);
+        }
+      }
+      const float mu = (mU == -INFINITY) ? 0.f : mU;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t hw[16], lw[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int k0 = 32 * c + 2 * e;
+          const float p0 = ex2(fmaf(sv[k0], fA, -mu));
+          const float p1 = ex2(fmaf(sv[k0 + 1], fA, -mu));
+          l += p0 + p1;
+          float vf0, vf1;
+          if constexpr (C::DYN) {
+            vf0 = vsm[k0] * fv;
+            vf1 = vsm[k0 + 1] * fv;
+          } else {
+            vf0 = vf1 = WSTATIC;
+          }
+          const float x0 = p0 * vf0, x1 = p1 * vf1;
+          const uint32_t h = pack_f16x2(x0, x1);
+          hw[e] = h;
+          lw[e] = pack_f16x2(x0 - f16_lo(h), x1 - f16_hi(h));
+        }
+        tmem_st16_nowait(tP + 16 * c, hw);
+        tmem_st16_nowait(tP + 32 + 16 * c, lw);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full[j]);
+    }
+    // ---- epilogue: out = O x unscale / l (rows without a query store nothing)
+    const bool fin = __all_sync(0xffffffffu, mbar_wait(o_fin, 0u));
+    if (ok && fin && !__any_sync(0xffffffffu, *s_abort)) {
+      tc_fence_after();
+      const float unscale = C::DYN ? pow2i(vexp - WKP) : vs_static * (1.f / WSTATIC);
+      const float f = l > 0.f ? unscale / l : 0.f;
+      const int h = r / QP, ii = r - h * QP;
+      float* dst = a.out + ((long long)(q0 + qbase + j * QP + ii) * a.Hq + g * G + h) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float v[32];
+        tmem_ld32(tO + c0, v);
+        if (pA >= 0) {
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4)
+            *reinterpret_cast<float4*>(dst + c0 + 4 * i4) =
+                make_float4(v[4 * i4] * f, v[4 * i4 + 1] * f, v[4 * i4 + 2] * f, v[4 * i4 + 3] * f);
+        }
+      }
+    }
+  }
+
+  // ---- tensor memory is freed once every role is done with it
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(C::TCOLS));
+  }
+}
+
+template <int MODE, int D, int G>
+cudaError_t wslaunch3(const PrefillArgs& pa0, int max_query_len, cudaStream_t st) {
+  using C = WCfg<MODE, D>;
+  const DecodeArgs& a = pa0.d;
+  const long long total = a.num_blocks * a.Hkv * a.bs * (long long)C::RB;
+  CUtensorMap km, vm;
+  if (total > 0) {
+    if (!make_tile_map(&km, a.k_cache, total, C::TB) || !make_tile_map(&vm, a.v_cache, total, C::TB))
+      return cudaErrorInvalidValue;
+  }
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  auto kern = prefill_ws_kernel<MODE, D, G>;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  PrefillArgs pa = pa0;
+  const int qp2 = 2 * (WROWS / G);                  // query positions per CTA
+  pa.qtiles = (max_query_len + qp2 - 1) / qp2;
+  const long long grid = (long long)pa.qtiles * a.B * a.Hkv;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<(unsigned)grid, WS_THREADS, C::SMEM, st>>>(pa, km, vm);
+  return cudaGetLastError();
+}
+
+template <int MODE, int D>
+cudaError_t wslaunch2(int G, const PrefillArgs& pa, int mq, cudaStream_t st) {
+  switch (G) {
+    case 1: return wslaunch3<MODE, D, 1>(pa, mq, st);
+    case 2: return wslaunch3<MODE, D, 2>(pa, mq, st);
+    case 4: return wslaunch3<MODE, D, 4>(pa, mq, st);
+    case 8: return wslaunch3<MODE, D, 8>(pa, mq, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int MODE>
+cudaError_t wslaunch1(int D, int G, const PrefillArgs& pa, int mq, cudaStream_t st) {
+  switch (D) {
+    case 64: return wslaunch2<MODE, 64>(G, pa, mq, st);
+    case 128: return wslaunch2<MODE, 128>(G, pa, mq, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+bool prefill_ws_supports(int mode, int D) { return mode != BF16 && (D == 64 || D == 128); }
+
+cudaError_t launch_prefill_ws(int mode, int D, int G, const DecodeArgs& a, const int* query_start,
+                              int max_query_len, cudaStream_t st) {
+  if (a.B == 0 || max_query_len <= 0) return cudaSuccess;
+  PrefillArgs pa;
+  pa.d = a;
+  pa.query_start = query_start;
+  pa.qtiles = 0;
+  switch (mode) {
+    case FP8_PER_TENSOR: return wslaunch1<FP8_PER_TENSOR>(D, G, pa, max_query_len, st);
+    case FP8_PER_HEAD: return wslaunch1<FP8_PER_HEAD>(D, G, pa, max_query_len, st);
+    case FP8_PER_TOKEN_HEAD: return wslaunch1<FP8_PER_TOKEN_HEAD>(D, G, pa, max_query_len, st);
+    case INT4_PER_TOKEN_HEAD: return wslaunch1<INT4_PER_TOKEN_HEAD>(D, G, pa, max_query_len, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvq
