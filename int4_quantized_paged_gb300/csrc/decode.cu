@@ -37,9 +37,10 @@
 //    query's E4M3 values are f16 values).  Columns are the G query heads of
 //    the KV head, repeated once per term of the weight split when they fit
 //    in the 8 columns, so a QK column is already the PV column it feeds.
-//  * Online softmax in log2 units on the fragments (running max over the raw
-//    scores, reduced over the warp only on tiles where some lane holds a
-//    larger score).  The weights that meet V are P' = p * v_scale * 2^k, with k a
+//  * Online softmax in log2 units on the fragments, against a reference max
+//    that moves (reduced over the warp, O and l rescaled) only on tiles where
+//    some lane holds a score above it by more than 8 (a weight factor of
+//    2^8), so the weights p stay below 2^8.  The weights that meet V are P' = p * v_scale * 2^k, with k a
 //    power-of-two range factor that keeps P' below 2^14, so both f16 terms of
 //    its split stay normal numbers.
 //  * PV on tensor cores with d as the M dimension: O^T[d x cols] += V^T P'.
@@ -68,7 +69,12 @@ constexpr int WARPS = 4;         // worker warps per CTA (independent)
 #define KVQ_QK2 1
 #endif
 constexpr int TILE = 16;         // positions per tile
-constexpr int KP = 13;           // P' = p v_scale 2^(KP - vexp) < 2^14 (dynamic scales)
+// The reference max m_run a column's weights are taken against moves only
+// when a tile's score exceeds it by more than LAZY (log2 units), so most
+// tiles rescale nothing and the weights p stay below 2^LAZY.
+constexpr float LAZY = 8.f;
+constexpr int KP = 5;            // P' = p v_scale 2^(KP - vexp) < 2^14 (dynamic scales)
+constexpr float PSTATIC = 64.f;  // P' = p x 64 < 2^14 (static FP8 scales)
 
 template <int N>
 __device__ __forceinline__ void lds(uint32_t (&r)[N], const uint8_t* base, uint32_t o) {
@@ -602,6 +608,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
   uint32_t qf[C::KSTEPS][2];
   float s_fac = 0.f;
   float m_run[2], l_run[2];
+  float m_ref[2] = {0.f, 0.f};    // m_run, or 0 while it is -inf (every score so far -inf)
   float acc[NT][C::MTILES][4];
   int vexp = -1000;               // running max exponent of the V scales (dynamic)
   float fv = 0.f;                 // 2^(KP - vexp)
@@ -652,7 +659,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     float unscale;
     if constexpr (C::BF) unscale = 1.f;
     else if constexpr (C::DYN) unscale = pow2i(vexp - KP);
-    else unscale = vsg * (1.f / 16384.f);
+    else unscale = vsg * (1.f / PSTATIC);
     const int nh = (G == 1) ? 1 : 2;              // heads owned by this lane column
     const bool owner = (G == 1) ? (lt == 0) : (2 * lt < G);
     const bool full = (seg_k0 == 0 && seg_klast == seg_n - 1);
@@ -763,6 +770,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
       sq[0] = s_fac * qc[0];
       sq[1] = s_fac * qc[1];
       m_run[0] = m_run[1] = -INFINITY;
+      m_ref[0] = m_ref[1] = 0.f;
       l_run[0] = l_run[1] = 0.f;
       vexp = -1000;
       fv = 0.f;
@@ -823,12 +831,13 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
       }
     }
 
-    // ---------------- online softmax.  The running max m_run (per column,
-    // warp-uniform) and the V-scale exponent vexp only change when some lane
-    // holds a larger value; only then are they reduced over the warp and O
+    // ---------------- online softmax.  The reference max m_run (per column,
+    // warp-uniform) moves only when some lane holds a score above it by more
+    // than LAZY, and the V-scale exponent vexp only when a retained V scale
+    // reaches 2^(vexp + 1); only then are they reduced over the warp and O
     // and l rescaled, so most tiles take no shuffle here.
     const float lmax[2] = {fmaxf(s_raw[0], s_raw[2]), fmaxf(s_raw[1], s_raw[3])};
-    const bool raise = lmax[0] > m_run[0] || lmax[1] > m_run[1] || vraise;
+    const bool raise = lmax[0] > m_run[0] + LAZY || lmax[1] > m_run[1] + LAZY || vraise;
     if (__any_sync(0xffffffffu, raise)) {
       float al[2];
 #pragma unroll
@@ -840,6 +849,7 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
         al[c] = (mn == -INFINITY) ? 1.f : ex2(m_run[c] - mn);   // 0 while m_run is -inf
         l_run[c] *= al[c];
         m_run[c] = mn;
+        m_ref[c] = (mn == -INFINITY) ? 0.f : mn;
       }
       if constexpr (C::DYN) {
         int et = -1000;                 // largest V-scale exponent of the retained rows
@@ -873,19 +883,17 @@ __global__ void __launch_bounds__(WARPS * 32, MinCtas<MODE, D, G>::value)
     float pw[4];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      // m_run is -inf only while every score so far is -inf: weights 0
-      const float mu = (m_run[c] == -INFINITY) ? 0.f : m_run[c];
-      pw[c] = ex2(s_raw[c] - mu);
-      pw[c + 2] = ex2(s_raw[c + 2] - mu);
+      pw[c] = ex2(s_raw[c] - m_ref[c]);
+      pw[c + 2] = ex2(s_raw[c + 2] - m_ref[c]);
       l_run[c] += pw[c] + pw[c + 2];
     }
-    // weights that meet V: P' = p v_scale 2^(KP - vexp) (dynamic), p 2^14 (FP8)
+    // weights that meet V: P' = p v_scale 2^(KP - vexp) (dynamic), p 64 (FP8)
     if constexpr (C::DYN) {
       const float f0 = vs0 * fv, f1 = vs1 * fv;
       pw[0] *= f0; pw[1] *= f0; pw[2] *= f1; pw[3] *= f1;
     } else if constexpr (!C::BF) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) pw[e] *= 16384.f;
+      for (int e = 0; e < 4; ++e) pw[e] *= PSTATIC;
     }
 
     // ---------------- PV
