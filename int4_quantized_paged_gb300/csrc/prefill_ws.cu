@@ -57,7 +57,7 @@ constexpr int WROWS = 128;                          // rows per query tile (the 
 constexpr int WKT = 64;                             // keys per tile
 constexpr int WKP = 6;                              // P' = p v_scale 2^(WKP - vexp) < 2^15 (p <= 2^8)
 constexpr float WLAZY = 8.f;                        // the reference max moves when exceeded by this
-constexpr float WSTATIC = 64.f;                     // P' = p x 64 for static FP8 scales (< 2^14)
+// static FP8 scales: P' = p x 2^6 (< 2^14)
 constexpr int CONV_BAR = 1;                         // named barrier of the converter warps
 
 template <int MODE, int D>
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     for (int i = 0; i < ntl; ++i) {
       const int st = i % NR;
       if (i >= NR) {
-        const bool ok = mbar_wait(&raw_empty[st], (uint32_t)((i / NR - 1) & 1));
+        const bool ok = mbar_wait_sleep(&raw_empty[st], (uint32_t)((i / NR - 1) & 1));
         if (!__all_sync(0xffffffffu, ok)) {
           if (lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
           break;
@@ -279,15 +279,15 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     if (lane == 0)
 #pragma unroll
       for (int s = 0; s < NR; ++s)
-        if (last[s] >= 0) (void)mbar_wait(&raw_full[s], (uint32_t)((last[s] / NR) & 1));
+        if (last[s] >= 0) (void)mbar_wait_sleep(&raw_full[s], (uint32_t)((last[s] / NR) & 1));
   } else if (warp >= WS_SOFT && warp < WS_PROD) {
     // ---- converters (128 threads)
     const int ct_ = tid - WS_SOFT * 32;
     for (int i = 0; i < ntl; ++i) {
       const int st = i % NR, buf = i & 1;
       const int t = t0 + i;
-      bool ok = mbar_wait(&raw_full[st], (uint32_t)((i / NR) & 1));
-      if (i >= 2) ok = mbar_wait(&kv_empty[buf], (uint32_t)((i / 2 - 1) & 1)) && ok;
+      bool ok = mbar_wait_sleep(&raw_full[st], (uint32_t)((i / NR) & 1));
+      if (i >= 2) ok = mbar_wait_sleep(&kv_empty[buf], (uint32_t)((i / 2 - 1) & 1)) && ok;
       if (!ok) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
       // every converter thread takes the same decision (a barrier reduction)
       if (named_sync_or(CONV_BAR, WS_CONV * 32, !ok || *s_abort)) break;
@@ -295,29 +295,36 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       const uint8_t* base = raw + st * C::RAWS;
       uint8_t* kb = k16 + buf * C::KB;
       // K into kb, V into the row-major staging copy (zeros where nothing was
-      // fetched or the position lies outside [kmin, pmax])
-      for (int c = ct_; c < 2 * WKT * CPR; c += WS_CONV * 32) {
-        const int isv = c >= WKT * CPR;
-        const int cc = isv ? c - WKT * CPR : c;
-        const int key = cc / CPR, ch = cc - key * CPR;
+      // fetched or the position lies outside [kmin, pmax]).  Each thread takes
+      // NIT chunks of K and as many of V; all loads first, then conversions.
+      constexpr int NIT = WKT * CPR / (WS_CONV * 32);
+      static_assert(NIT * WS_CONV * 32 == WKT * CPR, "chunks per converter thread");
+      uint4 wk[NIT], wv[NIT];
+#pragma unroll
+      for (int it = 0; it < NIT; ++it) {
+        const int cc = ct_ + it * WS_CONV * 32;
+        const int key = cc / CPR, ch = cc % CPR;
         const int sub = key >> 4, kr = key & 15;
         const int pos = t * WKT + key;
         const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (live)
-          w = *reinterpret_cast<const uint4*>(base + (isv ? SUB + sub : sub) * C::TBP +
-                                             swz((uint32_t)(kr * C::RB + ch * 16)));
-        uint4 o[4];
-        convert16<MODE>(w, o);
-        constexpr int NCH = EPC / 8;
-        const int d0 = ch * EPC;
+        const uint32_t off = swz((uint32_t)(kr * C::RB + ch * 16));
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        wk[it] = live ? *reinterpret_cast<const uint4*>(base + sub * C::TBP + off) : z;
+        wv[it] = live ? *reinterpret_cast<const uint4*>(base + (SUB + sub) * C::TBP + off) : z;
+      }
 #pragma unroll
-        for (int qq = 0; qq < NCH; ++qq) {
+      for (int it = 0; it < NIT; ++it) {
+        const int cc = ct_ + it * WS_CONV * 32;
+        const int key = cc / CPR, ch = cc % CPR;
+        const int d0 = ch * EPC;
+        uint4 ok_[4], ov[4];
+        convert16<MODE>(wk[it], ok_);
+        convert16<MODE>(wv[it], ov);
+#pragma unroll
+        for (int qq = 0; qq < EPC / 8; ++qq) {
           const int d = d0 + 8 * qq;
-          if (isv)
-            *reinterpret_cast<uint4*>(stg + key * C::LDV + d * 2) = o[qq];
-          else
-            *reinterpret_cast<uint4*>(kb + (d >> 6) * (WKT * 128) + swc(key, (d & 63) >> 3)) = o[qq];
+          *reinterpret_cast<uint4*>(kb + (d >> 6) * (WKT * 128) + swc(key, (d & 63) >> 3)) = ok_[qq];
+          *reinterpret_cast<uint4*>(stg + key * C::LDV + d * 2) = ov[qq];
         }
       }
       {
@@ -347,7 +354,11 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       if (ct_ == 0) mbar_arrive(&raw_empty[st]);
       // V^T: rows d, chunks of 8 keys, from the staging copy
       uint8_t* vb = vt16 + buf * C::VTB;
-      for (int u = ct_; u < (WKT / 8) * (D / 2); u += WS_CONV * 32) {
+      constexpr int NVT = (WKT / 8) * (D / 2) / (WS_CONV * 32);
+      static_assert(NVT * WS_CONV * 32 == (WKT / 8) * (D / 2), "V^T tasks per converter thread");
+#pragma unroll
+      for (int it = 0; it < NVT; ++it) {
+        const int u = ct_ + it * WS_CONV * 32;
         const int dp = u % (D / 2), kg = u / (D / 2);
         uint32_t wv[8];
 #pragma unroll
@@ -370,41 +381,46 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       if (ct_ == 0) mbar_arrive(&kv_full[buf]);
     }
   } else if (warp == WS_MMA) {
-    // ---- MMA issuer: lane 0 issues and commits; the warp waits together
+    // ---- MMA issuer: one elected lane issues and commits (elect.sync picks
+    // the same lane each time: the warp is converged); the warp waits together
     constexpr uint32_t IDS = mma_idesc<false>(WROWS, WKT);
     constexpr uint32_t IDO = mma_idesc<false>(WROWS, D);
     auto wait = [&](uint64_t* bar, uint32_t par) -> bool {
-      const bool w = __all_sync(0xffffffffu, mbar_wait(bar, par));
+      const bool w = __all_sync(0xffffffffu, mbar_wait_sleep(bar, par));
       if (!w && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
       return w && !__any_sync(0xffffffffu, *s_abort);
     };
+    // Descriptors of the operand buffers' starts; an operand at byte offset
+    // o is the start's descriptor plus o / 16 (the 14-bit address field
+    // cannot carry: shared memory ends below 2^18 bytes)
+    const uint64_t dq = sw128_desc(q16), dk = sw128_desc(k16), dv = sw128_desc(vt16);
     // S_j = Q_j K^T from K buffer kbuf
     auto issue_s = [&](int j, int kbuf) {
-      if (lane == 0) {
+      const uint64_t qa = dq + (uint64_t)(j * (C::QB >> 4));
+      const uint64_t kb = dk + (uint64_t)(kbuf * (C::KB >> 4));
+      const uint32_t td = tmem + C::SCOL + 64 * j;
+      if (elect_one()) {
         tc_fence_after();
-        const uint8_t* qa = q16 + j * C::QB;
-        const uint8_t* kb = k16 + kbuf * C::KB;
 #pragma unroll
-        for (int s2 = 0; s2 < D / 16; ++s2) {
-          const uint64_t da = sw128_desc(qa + (s2 >> 2) * (WROWS * 128) + (s2 & 3) * 32);
-          const uint64_t db = sw128_desc(kb + (s2 >> 2) * (WKT * 128) + (s2 & 3) * 32);
-          umma(tmem + C::SCOL + 64 * j, da, db, IDS, s2 > 0);
-        }
+        for (int s2 = 0; s2 < D / 16; ++s2)
+          umma(td, qa + (uint64_t)((((s2 >> 2) * (WROWS * 128)) + (s2 & 3) * 32) >> 4),
+               kb + (uint64_t)((((s2 >> 2) * (WKT * 128)) + (s2 & 3) * 32) >> 4), IDS, s2 > 0);
         umma_commit(&s_full[j]);
       }
       __syncwarp();
     };
     // O_j += P'_j V, both terms of the split, V^T from buffer vbuf
     auto issue_pv = [&](int j, int vbuf, bool acc) {
-      if (lane == 0) {
+      const uint64_t vb = dv + (uint64_t)(vbuf * (C::VTB >> 4));
+      const uint32_t td = tmem + C::OCOL + D * j;
+      const uint32_t ta = tmem + C::PCOL + 64 * j;
+      if (elect_one()) {
         tc_fence_after();
-        const uint8_t* vb = vt16 + vbuf * C::VTB;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int kk = 0; kk < WKT / 16; ++kk)
-            umma_tmem_a(tmem + C::OCOL + D * j, tmem + C::PCOL + 64 * j + 32 * h + 8 * kk,
-                        sw128_desc(vb + kk * 32), IDO, acc || h > 0 || kk > 0);
+            umma_tmem_a(td, ta + 32 * h + 8 * kk, vb + (uint64_t)(kk * 2), IDO, acc || h > 0 || kk > 0);
       }
       __syncwarp();
     };
@@ -423,15 +439,15 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
         if (!wait(&p_full[1], (uint32_t)(i & 1))) break;
         issue_pv(1, buf, i > 0);
         // both PVs of this key tile have read its operands: buffer free
-        if (lane == 0) umma_commit(&kv_empty[buf]);
+        if (elect_one()) umma_commit(&kv_empty[buf]);
         __syncwarp();
         if (more) issue_s(1, buf ^ 1);
       }
     }
     // everything issued completes before the epilogue and the exit
-    if (lane == 0) umma_commit(o_fin);
+    if (elect_one()) umma_commit(o_fin);
     __syncwarp();
-    (void)mbar_wait(o_fin, 0u);
+    (void)mbar_wait_sleep(o_fin, 0u);
   } else {
     // ---- softmax of query tile j: one thread per row (its tensor-memory lane)
     const int j = warp >> 2;
@@ -453,14 +469,13 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     // rescaled rarely and the weights stay below 2^WLAZY
     float mU = -INFINITY, l = 0.f;
     int vexp = -1000;
-    float fv = 0.f;                                  // 2^(WKP - vexp)
     float vs_static = 1.f;
     if constexpr (MODE == FP8_PER_TENSOR) vs_static = a.v_scale[0];
     if constexpr (MODE == FP8_PER_HEAD) vs_static = a.v_scale[g];
     bool ok = true;
     for (int i = 0; i < ntl; ++i) {
       const int buf = i & 1, t = t0 + i;
-      const bool w = __all_sync(0xffffffffu, mbar_wait(&s_full[j], (uint32_t)(i & 1)));
+      const bool w = __all_sync(0xffffffffu, mbar_wait_sleep(&s_full[j], (uint32_t)(i & 1)));
       if (!w && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
       if (!w || __any_sync(0xffffffffu, *s_abort)) { ok = false; break; }
       tc_fence_after();
@@ -473,41 +488,60 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       const int* tinfo = reinterpret_cast<const int*>(vsm + WKT);
       const bool fast = tinfo[2] != 0 && t * WKT + WKT - 1 <= firstj &&
                         (a.window <= 0 || t * WKT >= pmaxj + 1 - a.window);
+      // scores times the K scale (or -inf where masked); four running maxima.
+      // The test for a wholly visible tile is taken once, outside the
+      // unrolled loops, so neither loop branches per key.
+      const float4* ks4 = reinterpret_cast<const float4*>(ksm);
       float sv[WKT];
-      float mt = -INFINITY;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (fast) {
 #pragma unroll
-      for (int k = 0; k < WKT; ++k) {
-        const float ks = ksm[k];
-        float x = __uint_as_float(k < 32 ? s0[k] : s1[k - 32]);
-        if (fast) {
-          x *= ks;
-        } else {
-          const int pos = t * WKT + k;
-          // a key outside the CTA's range or on a page not fetched has scale 0
-          const bool okk = pA >= 0 && pos >= loA && pos <= pA && ks != 0.f;
-          x = okk ? x * ks : -INFINITY;
+        for (int k4 = 0; k4 < WKT / 4; ++k4) {
+          const float4 kq = ks4[k4];
+          const float ksv[4] = {kq.x, kq.y, kq.z, kq.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k = 4 * k4 + e;
+            const float x = __uint_as_float(k < 32 ? s0[k] : s1[k - 32]) * ksv[e];
+            sv[k] = x;
+            m4[e] = fmaxf(m4[e], x);
+          }
         }
-        sv[k] = x;
-        mt = fmaxf(mt, x);
+      } else {
+        // keys of this row: [loA, pA] relative to the tile; a key outside the
+        // CTA's range or on a page not fetched has scale 0
+        const int klo = loA - t * WKT, khi = pA < 0 ? -1 : pA - t * WKT;
+#pragma unroll
+        for (int k4 = 0; k4 < WKT / 4; ++k4) {
+          const float4 kq = ks4[k4];
+          const float ksv[4] = {kq.x, kq.y, kq.z, kq.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k = 4 * k4 + e;
+            const bool okk = k >= klo && k <= khi && ksv[e] != 0.f;
+            const float x = okk ? __uint_as_float(k < 32 ? s0[k] : s1[k - 32]) * ksv[e] : -INFINITY;
+            sv[k] = x;
+            m4[e] = fmaxf(m4[e], x);
+          }
+        }
       }
-      const float mrow = mt * fA;
+      const float mrow = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * fA;
       float al = 1.f;
       if (mrow > mU + WLAZY || (mU == -INFINITY && mrow > -INFINITY)) {
         al = (mU == -INFINITY) ? 0.f : ex2(mU - mrow);
         mU = mrow;
       }
-      // the sum of weights follows the max only; O (whose weights carry the
-      // V-scale factor 2^(WKP - vexp)) also follows the V-scale exponent
-      l *= al;
       if constexpr (C::DYN) {
         const int et = max(tinfo[0], tinfo[1]);     // the same for every row (same keys)
         const int vnew = max(vexp, max(et, -100));
         if (vnew != vexp) {
           al *= pow2i(vexp - vnew);                 // 0 on the first data (O is 0)
           vexp = vnew;
-          fv = pow2i(WKP - vexp);
         }
       }
+      // l and O both carry the range factor 2^(WKP - vexp) (64 for static
+      // scales), so both follow the max and the V-scale exponent
+      l *= al;
       // O holds data from the first PV on (its completion precedes S of this tile)
       if (i > 0 && __any_sync(0xffffffffu, al != 1.f)) {
 #pragma unroll 1
@@ -519,41 +553,48 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
           tmem_st32(tO + c0, v);
         }
       }
-      const float mu = (mU == -INFINITY) ? 0.f : mU;
+      // p x 2^k = 2^(score - (mU - k)): the power-of-two range factor k
+      // (WKP - vexp, or 6 for static scales) enters the exponent, exactly
+      const float mu = ((mU == -INFINITY) ? 0.f : mU) - (C::DYN ? (float)(WKP - vexp) : 6.f);
+      const float4* vs4 = reinterpret_cast<const float4*>(vsm);
+      float lp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t hw[16], lw[16];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t hw[8], lw[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int k0 = 32 * c + 2 * e;
-          const float p0 = ex2(fmaf(sv[k0], fA, -mu));
-          const float p1 = ex2(fmaf(sv[k0 + 1], fA, -mu));
-          l += p0 + p1;
-          float vf0, vf1;
-          if constexpr (C::DYN) {
-            vf0 = vsm[k0] * fv;
-            vf1 = vsm[k0 + 1] * fv;
-          } else {
-            vf0 = vf1 = WSTATIC;
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int k = 16 * c + 4 * q4;
+          float x[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[e] = ex2(fmaf(sv[k + e], fA, -mu));
+            lp[e] += x[e];
           }
-          const float x0 = p0 * vf0, x1 = p1 * vf1;
-          const uint32_t h = pack_f16x2(x0, x1);
-          hw[e] = h;
-          lw[e] = pack_f16x2(x0 - f16_lo(h), x1 - f16_hi(h));
+          if constexpr (C::DYN) {
+            const float4 vq = vs4[k >> 2];
+            x[0] *= vq.x; x[1] *= vq.y; x[2] *= vq.z; x[3] *= vq.w;
+          }
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const uint32_t h = pack_f16x2(x[2 * h2], x[2 * h2 + 1]);
+            hw[2 * q4 + h2] = h;
+            lw[2 * q4 + h2] = pack_f16x2(x[2 * h2] - f16_lo(h), x[2 * h2 + 1] - f16_hi(h));
+          }
         }
-        tmem_st16_nowait(tP + 16 * c, hw);
-        tmem_st16_nowait(tP + 32 + 16 * c, lw);
+        tmem_st8_nowait(tP + 8 * c, hw);
+        tmem_st8_nowait(tP + 32 + 8 * c, lw);
       }
+      l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[j]);
     }
     // ---- epilogue: out = O x unscale / l (rows without a query store nothing)
-    const bool fin = __all_sync(0xffffffffu, mbar_wait(o_fin, 0u));
+    const bool fin = __all_sync(0xffffffffu, mbar_wait_sleep(o_fin, 0u));
     if (ok && fin && !__any_sync(0xffffffffu, *s_abort)) {
       tc_fence_after();
-      const float unscale = C::DYN ? pow2i(vexp - WKP) : vs_static * (1.f / WSTATIC);
-      const float f = l > 0.f ? unscale / l : 0.f;
+      // O / l: the range factor cancels; static scales multiply by v_scale
+      const float f = l > 0.f ? (C::DYN ? 1.f : vs_static) / l : 0.f;
       const int h = r / QP, ii = r - h * QP;
       float* dst = a.out + ((long long)(q0 + qbase + j * QP + ii) * a.Hq + g * G + h) * D;
 #pragma unroll 1
