@@ -22,8 +22,10 @@
 //  * warp 13, MMA issuer (one thread): S_j = Q_j K^T (M 128, N 64) into
 //    tensor memory for each query tile j, and O_j += P'_j V with P'_j read
 //    from tensor memory, every term of its f16 hi + lo split.  Order per key
-//    tile t: PV_0(t), S_0(t+1), PV_1(t), S_1(t+1), so that the tensor cores
-//    work on one query tile while the softmax of the other runs.
+//    tile t: S_0(t+1), PV_0(t), S_1(t+1), PV_1(t), so that the tensor cores
+//    work on one query tile while the softmax of the other runs, and the
+//    softmax of t+1 starts while PV(t) runs (it waits for PV(t) only before
+//    it rescales O and overwrites P').
 //  * warps 0-3 and 4-7, softmax of query tile 0 and 1: one thread per row
 //    (its tensor-memory lane) loads the row's 64 scores, applies the K scale
 //    and masks, keeps a lazily moved reference max (moved only when a tile
@@ -80,8 +82,11 @@ struct WCfg {
   static constexpr int SCS = 2 * WKT * 4 + 16;
   static constexpr int ROWB = 2 * 2 * WROWS * 4;            // row factor and position per row
   static constexpr int BARB = 32 * 8;                       // barriers
-  static constexpr int FIXED = 2 * QB + 2 * KB + 2 * VTB + STG + 2 * SCS + ROWB + BARB + 64;
   static constexpr int LIMIT = 232448 - 1024;               // per-CTA shared memory, minus slack
+  // operand buffers (K, V^T, scales): three when they fit beside two raw stages
+  static constexpr int fixed_of(int nb) { return 2 * QB + nb * (KB + VTB + SCS) + STG + ROWB + BARB + 64; }
+  static constexpr int NB = (fixed_of(3) + 2 * RAWS <= LIMIT) ? 3 : 2;
+  static constexpr int FIXED = fixed_of(NB);
   static constexpr int NR = (FIXED + 4 * RAWS <= LIMIT) ? 4 : ((FIXED + 3 * RAWS <= LIMIT) ? 3 : 2);
   static constexpr int SMEM = NR * RAWS + FIXED + 1024;
   // tensor-memory columns
@@ -101,6 +106,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   const DecodeArgs& a = pa.d;
   constexpr int SUB = C::SUB;
   constexpr int NR = C::NR;
+  constexpr int NB = C::NB;
   constexpr int QP = WROWS / G;                // positions per query tile
   constexpr int CPR = C::RB / 16;              // 16-byte raw chunks per position row
   constexpr int EPC = (MODE == INT4_PER_TOKEN_HEAD) ? 32 : 16;   // elements per raw chunk
@@ -110,20 +116,21 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
                                              ~uintptr_t(1023));
   uint8_t* raw = smem;                                       // NR stages
   uint8_t* q16 = raw + NR * C::RAWS;                         // 2 query tiles
-  uint8_t* k16 = q16 + 2 * C::QB;                            // 2 K buffers
-  uint8_t* vt16 = k16 + 2 * C::KB;                           // 2 V^T buffers
-  uint8_t* stg = vt16 + 2 * C::VTB;                          // V staging copy
-  uint8_t* scb = stg + C::STG;                               // 2 scale buffers
-  float* rowf = reinterpret_cast<float*>(scb + 2 * C::SCS);  // [2][128] score factor per row
+  uint8_t* k16 = q16 + 2 * C::QB;                            // NB K buffers
+  uint8_t* vt16 = k16 + NB * C::KB;                          // NB V^T buffers
+  uint8_t* stg = vt16 + NB * C::VTB;                         // V staging copy
+  uint8_t* scb = stg + C::STG;                               // NB scale buffers
+  float* rowf = reinterpret_cast<float*>(scb + NB * C::SCS); // [2][128] score factor per row
   int* rowp = reinterpret_cast<int*>(rowf + 2 * WROWS);      // [2][128] position (-1: no row)
   uint64_t* bars = reinterpret_cast<uint64_t*>(rowp + 2 * WROWS);
   uint64_t* raw_full = bars;                                 // [NR] producer -> converters
   uint64_t* raw_empty = raw_full + NR;                       // [NR] converters -> producer
-  uint64_t* kv_full = raw_empty + NR;                        // [2] converters -> MMA
-  uint64_t* kv_empty = kv_full + 2;                          // [2] MMA (commit) -> converters
-  uint64_t* s_full = kv_empty + 2;                           // [2] MMA (commit) -> softmax j
+  uint64_t* kv_full = raw_empty + NR;                        // [NB] converters -> MMA
+  uint64_t* kv_empty = kv_full + NB;                         // [NB] MMA (commit) -> converters
+  uint64_t* s_full = kv_empty + NB;                          // [2] MMA (commit) -> softmax j
   uint64_t* p_full = s_full + 2;                             // [2] softmax j (128 arrivals) -> MMA
-  uint64_t* o_fin = p_full + 2;                              // MMA (commit) -> softmax, at the end
+  uint64_t* pv_done = p_full + 2;                            // [2] MMA (commit) -> softmax j
+  uint64_t* o_fin = pv_done + 2;                             // MMA (commit) -> softmax, at the end
   int* s_have = reinterpret_cast<int*>(bars + 32);           // [NR] fetched page tiles per stage
   volatile int* s_abort = s_have + 4;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_have + 5);
@@ -156,11 +163,14 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NB; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 4 * 32);
+      mbar_init(&pv_done[s], 1);
     }
     mbar_init(o_fin, 1);
     mbar_init_fence();
@@ -284,10 +294,10 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     // ---- converters (128 threads)
     const int ct_ = tid - WS_SOFT * 32;
     for (int i = 0; i < ntl; ++i) {
-      const int st = i % NR, buf = i & 1;
+      const int st = i % NR, buf = i % NB;
       const int t = t0 + i;
       bool ok = mbar_wait_sleep(&raw_full[st], (uint32_t)((i / NR) & 1));
-      if (i >= 2) ok = mbar_wait_sleep(&kv_empty[buf], (uint32_t)((i / 2 - 1) & 1)) && ok;
+      if (i >= NB) ok = mbar_wait_sleep(&kv_empty[buf], (uint32_t)((i / NB - 1) & 1)) && ok;
       if (!ok) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
       // every converter thread takes the same decision (a barrier reduction)
       if (named_sync_or(CONV_BAR, WS_CONV * 32, !ok || *s_abort)) break;
@@ -428,20 +438,28 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       issue_s(0, 0);
       issue_s(1, 0);
       for (int i = 0; i < ntl; ++i) {
-        const int buf = i & 1;
+        const int buf = i % NB, nbuf = (i + 1) % NB;
         const bool more = i + 1 < ntl;
+        // S_j(t+1) goes ahead of PV_j(t): the softmax of the next tile starts
+        // while PV_j(t) runs, and waits for it (pv_done) only before it
+        // rescales O_j and overwrites P'_j
         if (!wait(&p_full[0], (uint32_t)(i & 1))) break;
-        issue_pv(0, buf, i > 0);
         if (more) {
-          if (!wait(&kv_full[buf ^ 1], (uint32_t)(((i + 1) >> 1) & 1))) break;
-          issue_s(0, buf ^ 1);
+          if (!wait(&kv_full[nbuf], (uint32_t)(((i + 1) / NB) & 1))) break;
+          issue_s(0, nbuf);
         }
+        issue_pv(0, buf, i > 0);
+        if (elect_one()) umma_commit(&pv_done[0]);
+        __syncwarp();
         if (!wait(&p_full[1], (uint32_t)(i & 1))) break;
+        if (more) issue_s(1, nbuf);
         issue_pv(1, buf, i > 0);
         // both PVs of this key tile have read its operands: buffer free
-        if (elect_one()) umma_commit(&kv_empty[buf]);
+        if (elect_one()) {
+          umma_commit(&pv_done[1]);
+          umma_commit(&kv_empty[buf]);
+        }
         __syncwarp();
-        if (more) issue_s(1, buf ^ 1);
       }
     }
     // everything issued completes before the epilogue and the exit
@@ -474,7 +492,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     if constexpr (MODE == FP8_PER_HEAD) vs_static = a.v_scale[g];
     bool ok = true;
     for (int i = 0; i < ntl; ++i) {
-      const int buf = i & 1, t = t0 + i;
+      const int buf = i % NB, t = t0 + i;
       const bool w = __all_sync(0xffffffffu, mbar_wait_sleep(&s_full[j], (uint32_t)(i & 1)));
       if (!w && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
       if (!w || __any_sync(0xffffffffu, *s_abort)) { ok = false; break; }
@@ -542,7 +560,14 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       // l and O both carry the range factor 2^(WKP - vexp) (64 for static
       // scales), so both follow the max and the V-scale exponent
       l *= al;
-      // O holds data from the first PV on (its completion precedes S of this tile)
+      // the previous PV has read P'_j and updated O_j
+      if (i > 0) {
+        const bool w2 = __all_sync(0xffffffffu, mbar_wait_sleep(&pv_done[j], (uint32_t)((i - 1) & 1)));
+        if (!w2 && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
+        if (!w2 || __any_sync(0xffffffffu, *s_abort)) { ok = false; break; }
+        tc_fence_after();
+      }
+      // O holds data from the first PV on
       if (i > 0 && __any_sync(0xffffffffu, al != 1.f)) {
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
