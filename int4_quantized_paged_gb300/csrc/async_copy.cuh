@@ -44,31 +44,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// One try that may suspend the thread until the phase completes (or about a
-// millisecond passes): a waiting warp then takes no issue slots from the
-// warps it shares a scheduler with.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000; "
-      "selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// As mbar_wait, suspended rather than spinning while the phase is open.
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
-                                                long long limit = SPIN_LIMIT_CYCLES) {
-  if (mbar_try_wait_sleep(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait_sleep(bar, parity)) {
-    if (clock64() - t0 > limit) return false;
-  }
-  return true;
-}
-
 // Bounded wait; returns false when `limit` SM clock cycles ran out (the
 // kernels use SPIN_LIMIT_CYCLES; a shorter limit only serves the wait check).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,

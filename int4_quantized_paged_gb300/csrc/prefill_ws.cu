@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     for (int i = 0; i < ntl; ++i) {
       const int st = i % NR;
       if (i >= NR) {
-        const bool ok = mbar_wait_sleep(&raw_empty[st], (uint32_t)((i / NR - 1) & 1));
+        const bool ok = mbar_wait(&raw_empty[st], (uint32_t)((i / NR - 1) & 1));
         if (!__all_sync(0xffffffffu, ok)) {
           if (lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
           break;
@@ -289,15 +289,15 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     if (lane == 0)
 #pragma unroll
       for (int s = 0; s < NR; ++s)
-        if (last[s] >= 0) (void)mbar_wait_sleep(&raw_full[s], (uint32_t)((last[s] / NR) & 1));
+        if (last[s] >= 0) (void)mbar_wait(&raw_full[s], (uint32_t)((last[s] / NR) & 1));
   } else if (warp >= WS_SOFT && warp < WS_PROD) {
     // ---- converters (128 threads)
     const int ct_ = tid - WS_SOFT * 32;
     for (int i = 0; i < ntl; ++i) {
       const int st = i % NR, buf = i % NB;
       const int t = t0 + i;
-      bool ok = mbar_wait_sleep(&raw_full[st], (uint32_t)((i / NR) & 1));
-      if (i >= NB) ok = mbar_wait_sleep(&kv_empty[buf], (uint32_t)((i / NB - 1) & 1)) && ok;
+      bool ok = mbar_wait(&raw_full[st], (uint32_t)((i / NR) & 1));
+      if (i >= NB) ok = mbar_wait(&kv_empty[buf], (uint32_t)((i / NB - 1) & 1)) && ok;
       if (!ok) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
       // every converter thread takes the same decision (a barrier reduction)
       if (named_sync_or(CONV_BAR, WS_CONV * 32, !ok || *s_abort)) break;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     constexpr uint32_t IDS = mma_idesc<false>(WROWS, WKT);
     constexpr uint32_t IDO = mma_idesc<false>(WROWS, D);
     auto wait = [&](uint64_t* bar, uint32_t par) -> bool {
-      const bool w = __all_sync(0xffffffffu, mbar_wait_sleep(bar, par));
+      const bool w = __all_sync(0xffffffffu, mbar_wait(bar, par));
       if (!w && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
       return w && !__any_sync(0xffffffffu, *s_abort);
     };
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     // everything issued completes before the epilogue and the exit
     if (elect_one()) umma_commit(o_fin);
     __syncwarp();
-    (void)mbar_wait_sleep(o_fin, 0u);
+    (void)mbar_wait(o_fin, 0u);
   } else {
     // ---- softmax of query tile j: one thread per row (its tensor-memory lane)
     const int j = warp >> 2;
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     bool ok = true;
     for (int i = 0; i < ntl; ++i) {
       const int buf = i % NB, t = t0 + i;
-      const bool w = __all_sync(0xffffffffu, mbar_wait_sleep(&s_full[j], (uint32_t)(i & 1)));
+      const bool w = __all_sync(0xffffffffu, mbar_wait(&s_full[j], (uint32_t)(i & 1)));
       if (!w && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
       if (!w || __any_sync(0xffffffffu, *s_abort)) { ok = false; break; }
       tc_fence_after();
@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       l *= al;
       // the previous PV has read P'_j and updated O_j
       if (i > 0) {
-        const bool w2 = __all_sync(0xffffffffu, mbar_wait_sleep(&pv_done[j], (uint32_t)((i - 1) & 1)));
+        const bool w2 = __all_sync(0xffffffffu, mbar_wait(&pv_done[j], (uint32_t)((i - 1) & 1)));
         if (!w2 && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
         if (!w2 || __any_sync(0xffffffffu, *s_abort)) { ok = false; break; }
         tc_fence_after();
@@ -615,7 +615,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       mbar_arrive(&p_full[j]);
     }
     // ---- epilogue: out = O x unscale / l (rows without a query store nothing)
-    const bool fin = __all_sync(0xffffffffu, mbar_wait_sleep(o_fin, 0u));
+    const bool fin = __all_sync(0xffffffffu, mbar_wait(o_fin, 0u));
     if (ok && fin && !__any_sync(0xffffffffu, *s_abort)) {
       tc_fence_after();
       // O / l: the range factor cancels; static scales multiply by v_scale
