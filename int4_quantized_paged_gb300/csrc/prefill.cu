@@ -300,29 +300,40 @@ __global__ void __launch_bounds__(TWARPS * 32, 1)
     uint8_t* kb = k16;
     uint8_t* pb = p16;
     // K into kb, V into the row-major staging copy in pb (zeros where
-    // nothing was fetched or the position lies outside [kmin, pmax])
-    for (int c = tid; c < 2 * KT * CPR; c += TWARPS * 32) {
-      const int isv = c >= KT * CPR;
-      const int cc = isv ? c - KT * CPR : c;
-      const int key = cc / CPR, ch = cc - key * CPR;
-      const int sub = key >> 4, kr = key & 15;
-      const int pos = tt * KT + key;
-      const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (live)
-        w = *reinterpret_cast<const uint4*>(base + (isv ? SUB + sub : sub) * C::TBP +
-                                           swz((uint32_t)(kr * C::RB + ch * 16)));
-      uint4 o[4];
-      convert16<MODE>(w, o);
-      constexpr int NCH = EPC / 8;                 // output chunks of 8 elements
-      const int d0 = ch * EPC;
+    // nothing was fetched or the position lies outside [kmin, pmax]).  Each
+    // thread takes NIT chunks of K and as many of V; all loads first, then
+    // the conversions, with no branch per chunk.
+    // (INT4 at D 64 has fewer chunks than threads: the rest idle, whole warps)
+    constexpr int NIT = (KT * CPR + TWARPS * 32 - 1) / (TWARPS * 32);
+    {
+      uint4 wk[NIT], wv[NIT];
 #pragma unroll
-      for (int q = 0; q < NCH; ++q) {
-        const int d = d0 + 8 * q;
-        if (isv)
-          *reinterpret_cast<uint4*>(pb + key * C::LDV + d * 2) = o[q];
-        else
-          *reinterpret_cast<uint4*>(kb + (d >> 6) * (KT * 128) + swc(key, (d & 63) >> 3)) = o[q];
+      for (int it = 0; it < NIT; ++it) {
+        const int cc = tid + it * TWARPS * 32;
+        const int key = cc / CPR, ch = cc % CPR;
+        const int sub = key >> 4, kr = key & 15;
+        const int pos = tt * KT + key;
+        const bool live = cc < KT * CPR && ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
+        const uint32_t off = swz((uint32_t)(kr * C::RB + ch * 16));
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        wk[it] = live ? *reinterpret_cast<const uint4*>(base + sub * C::TBP + off) : z;
+        wv[it] = live ? *reinterpret_cast<const uint4*>(base + (SUB + sub) * C::TBP + off) : z;
+      }
+#pragma unroll
+      for (int it = 0; it < NIT; ++it) {
+        const int cc = tid + it * TWARPS * 32;
+        if (cc >= KT * CPR) break;
+        const int key = cc / CPR, ch = cc % CPR;
+        uint4 ok_[4], ov[4];
+        convert16<MODE>(wk[it], ok_);
+        convert16<MODE>(wv[it], ov);
+        const int d0 = ch * EPC;
+#pragma unroll
+        for (int q = 0; q < EPC / 8; ++q) {
+          const int d = d0 + 8 * q;
+          *reinterpret_cast<uint4*>(kb + (d >> 6) * (KT * 128) + swc(key, (d & 63) >> 3)) = ok_[q];
+          *reinterpret_cast<uint4*>(pb + key * C::LDV + d * 2) = ov[q];
+        }
       }
     }
     if (tid < 2 * KT) {
@@ -352,7 +363,11 @@ __global__ void __launch_bounds__(TWARPS * 32, 1)
     }
     // V^T: rows d, chunks of 8 keys, from the staging copy
     uint8_t* vb = vt16;
-    for (int u = tid; u < (KT / 8) * (D / 2); u += TWARPS * 32) {
+    constexpr int NVT = (KT / 8) * (D / 2) / (TWARPS * 32);
+    static_assert(NVT * TWARPS * 32 == (KT / 8) * (D / 2), "V^T tasks per thread");
+#pragma unroll
+    for (int it = 0; it < NVT; ++it) {
+      const int u = tid + it * TWARPS * 32;
       const int dp = u % (D / 2), kg = u / (D / 2);
       uint32_t wv[8];
 #pragma unroll
@@ -373,7 +388,7 @@ __global__ void __launch_bounds__(TWARPS * 32, 1)
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
+    if (warp == 0 && elect_one()) {               // lane 0 of the converged warp 0
       tc_fence_after();
 #pragma unroll
       for (int s2 = 0; s2 < D / 16; ++s2) {
@@ -408,21 +423,29 @@ __global__ void __launch_bounds__(TWARPS * 32, 1)
       } else {
         tmem_ld16(trow + half * KH, sv);
       }
-      float mt = -INFINITY;
+      // the test for a wholly visible tile is taken once, outside the
+      // unrolled loops, so neither loop branches per key
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (fast) {
 #pragma unroll
-      for (int j = 0; j < KH; ++j) {
-        const int key = half * KH + j;
-        const float ks = kss[key];
-        if (fast) {
-          sv[j] *= ks;
-        } else {
-          const int pos = t * KT + key;
-          // a key whose page was not fetched (bad block id) has scale 0: masked
-          const bool okj = pA >= 0 && pos >= loA && pos <= pA && ks != 0.f;
-          sv[j] = okj ? sv[j] * ks : -INFINITY;
+        for (int j = 0; j < KH; ++j) {
+          sv[j] *= kss[half * KH + j];
+          m4[j & 3] = fmaxf(m4[j & 3], sv[j]);
         }
-        mt = fmaxf(mt, sv[j]);
+      } else {
+        // keys of this row relative to the tile; a key whose page was not
+        // fetched (bad block id) has scale 0: masked
+        const int klo = loA - t * KT, khi = pA < 0 ? -1 : pA - t * KT;
+#pragma unroll
+        for (int j = 0; j < KH; ++j) {
+          const int key = half * KH + j;
+          const float ks = kss[key];
+          const bool okj = key >= klo && key <= khi && ks != 0.f;
+          sv[j] = okj ? sv[j] * ks : -INFINITY;
+          m4[j & 3] = fmaxf(m4[j & 3], sv[j]);
+        }
       }
+      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       mx[half * TROWS + r] = mt;
     }
     if (__syncthreads_or(!sok)) {
@@ -505,7 +528,7 @@ __global__ void __launch_bounds__(TWARPS * 32, 1)
     }
     __syncthreads();
     // ---- O += P' V^T, every term of the split
-    if (tid == 0) {
+    if (warp == 0 && elect_one()) {
       tc_fence_after();
       const uint8_t* pb = p16;
       const uint8_t* vb = vt16;
