@@ -21,18 +21,20 @@
 //    tile's largest V-scale exponent.  Two operand buffers.
 //  * warp 13, MMA issuer (one thread): S_j = Q_j K^T (M 128, N 64) into
 //    tensor memory for each query tile j, and O_j += P'_j V with P'_j read
-//    from tensor memory, every term of its f16 hi + lo split.  Order per key
-//    tile t: S_0(t+1), PV_0(t), S_1(t+1), PV_1(t), so that the tensor cores
-//    work on one query tile while the softmax of the other runs, and the
-//    softmax of t+1 starts while PV(t) runs (it waits for PV(t) only before
-//    it rescales O and overwrites P').
+//    from tensor memory, every term of its f16 hi + lo split.  Each query
+//    tile has two S/P' buffers (key tile t uses buffer t & 1; P' replaces S
+//    there).  Order per key tile t: PV_0(t), PV_1(t), then S_0(t+2) and
+//    S_1(t+2) once the PV that last read each buffer has completed, so a
+//    softmax warpgroup finds the scores of its next tile ready and the
+//    tensor cores work on one query tile while the other's softmax runs.
 //  * warps 0-3 and 4-7, softmax of query tile 0 and 1: one thread per row
 //    (its tensor-memory lane) loads the row's 64 scores, applies the K scale
 //    and masks, keeps a lazily moved reference max (moved only when a tile
 //    exceeds it by more than 2^8), rescales the row of O in tensor memory
-//    when it moves, and stores P' = p x v_scale x 2^k (f16 hi + lo) into the
-//    query tile's own P' columns of tensor memory.
-// Tensor memory: S_0, S_1, P'_0, P'_1 (64 columns each), O_0, O_1 (D each).
+//    when it moves, and stores P' = p x v_scale x 2^k (f16 hi + lo) over the
+//    scores it has read.
+// Tensor memory: two S/P' buffers per query tile (64 columns each), O_0, O_1
+// (D each).
 // Every wait is bounded; a wait that runs out flags TIMEOUT and sets a
 // shared abort flag that ends every role's loop, the work already issued is
 // waited for (bounded again), and tensor memory is freed before the CTA exits.
@@ -90,8 +92,8 @@ struct WCfg {
   static constexpr int NR = (FIXED + 4 * RAWS <= LIMIT) ? 4 : ((FIXED + 3 * RAWS <= LIMIT) ? 3 : 2);
   static constexpr int SMEM = NR * RAWS + FIXED + 1024;
   // tensor-memory columns
-  static constexpr int SCOL = 0;                            // S_j at 64 j
-  static constexpr int PCOL = 128;                          // P'_j at 128 + 64 j (hi 32, lo 32)
+  // S/P' buffer b of query tile j at 64 (2 j + b): S (fp32, 64 columns),
+  // then P' (f16 hi in the first 32 columns, lo in the next 32) in its place
   static constexpr int OCOL = 256;                          // O_j at 256 + D j
   static constexpr int TCOLS = 512;
   static_assert(OCOL + 2 * D <= TCOLS, "tensor memory");
@@ -127,8 +129,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   uint64_t* raw_empty = raw_full + NR;                       // [NR] converters -> producer
   uint64_t* kv_full = raw_empty + NR;                        // [NB] converters -> MMA
   uint64_t* kv_empty = kv_full + NB;                         // [NB] MMA (commit) -> converters
-  uint64_t* s_full = kv_empty + NB;                          // [2] MMA (commit) -> softmax j
-  uint64_t* p_full = s_full + 2;                             // [2] softmax j (128 arrivals) -> MMA
+  uint64_t* s_full = kv_empty + NB;                          // [2][2] MMA (commit) -> softmax j, per S buffer
+  uint64_t* p_full = s_full + 4;                             // [2] softmax j (128 arrivals) -> MMA
   uint64_t* pv_done = p_full + 2;                            // [2] MMA (commit) -> softmax j
   uint64_t* o_fin = pv_done + 2;                             // MMA (commit) -> softmax, at the end
   int* s_have = reinterpret_cast<int*>(bars + 32);           // [NR] fetched page tiles per stage
@@ -167,8 +169,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(&s_full[s], 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 4 * 32);
       mbar_init(&pv_done[s], 1);
     }
@@ -404,26 +406,27 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     // o is the start's descriptor plus o / 16 (the 14-bit address field
     // cannot carry: shared memory ends below 2^18 bytes)
     const uint64_t dq = sw128_desc(q16), dk = sw128_desc(k16), dv = sw128_desc(vt16);
-    // S_j = Q_j K^T from K buffer kbuf
-    auto issue_s = [&](int j, int kbuf) {
+    // S_j = Q_j K^T from K buffer kbuf into S buffer sb of query tile j
+    auto issue_s = [&](int j, int kbuf, int sb) {
       const uint64_t qa = dq + (uint64_t)(j * (C::QB >> 4));
       const uint64_t kb = dk + (uint64_t)(kbuf * (C::KB >> 4));
-      const uint32_t td = tmem + C::SCOL + 64 * j;
+      const uint32_t td = tmem + 64 * (2 * j + sb);
       if (elect_one()) {
         tc_fence_after();
 #pragma unroll
         for (int s2 = 0; s2 < D / 16; ++s2)
           umma(td, qa + (uint64_t)((((s2 >> 2) * (WROWS * 128)) + (s2 & 3) * 32) >> 4),
                kb + (uint64_t)((((s2 >> 2) * (WKT * 128)) + (s2 & 3) * 32) >> 4), IDS, s2 > 0);
-        umma_commit(&s_full[j]);
+        umma_commit(&s_full[2 * j + sb]);
       }
       __syncwarp();
     };
-    // O_j += P'_j V, both terms of the split, V^T from buffer vbuf
-    auto issue_pv = [&](int j, int vbuf, bool acc) {
+    // O_j += P'_j V, both terms of the split, P' from S/P' buffer sb, V^T
+    // from buffer vbuf
+    auto issue_pv = [&](int j, int vbuf, int sb, bool acc) {
       const uint64_t vb = dv + (uint64_t)(vbuf * (C::VTB >> 4));
       const uint32_t td = tmem + C::OCOL + D * j;
-      const uint32_t ta = tmem + C::PCOL + 64 * j;
+      const uint32_t ta = tmem + 64 * (2 * j + sb);
       if (elect_one()) {
         tc_fence_after();
 #pragma unroll
@@ -434,32 +437,43 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       }
       __syncwarp();
     };
+    // S of key tile t goes into S/P' buffer t & 1 of each query tile, two
+    // tiles ahead of the softmax that reads it: S_j(t+2) is issued once
+    // PV_j(t), the last reader of that buffer's P', has completed, so the
+    // softmax of a query tile finds its next scores ready when it finishes
     if (wait(&kv_full[0], 0u)) {
-      issue_s(0, 0);
-      issue_s(1, 0);
-      for (int i = 0; i < ntl; ++i) {
-        const int buf = i % NB, nbuf = (i + 1) % NB;
-        const bool more = i + 1 < ntl;
-        // S_j(t+1) goes ahead of PV_j(t): the softmax of the next tile starts
-        // while PV_j(t) runs, and waits for it (pv_done) only before it
-        // rescales O_j and overwrites P'_j
-        if (!wait(&p_full[0], (uint32_t)(i & 1))) break;
-        if (more) {
-          if (!wait(&kv_full[nbuf], (uint32_t)(((i + 1) / NB) & 1))) break;
-          issue_s(0, nbuf);
+      issue_s(0, 0, 0);
+      issue_s(1, 0, 0);
+      bool go = true;
+      if (ntl > 1) {
+        go = wait(&kv_full[1 % NB], (uint32_t)((1 / NB) & 1));
+        if (go) {
+          issue_s(0, 1 % NB, 1);
+          issue_s(1, 1 % NB, 1);
         }
-        issue_pv(0, buf, i > 0);
+      }
+      for (int i = 0; go && i < ntl; ++i) {
+        const int buf = i % NB, sb = i & 1;
+        if (!wait(&p_full[0], (uint32_t)(i & 1))) break;
+        issue_pv(0, buf, sb, i > 0);
         if (elect_one()) umma_commit(&pv_done[0]);
         __syncwarp();
         if (!wait(&p_full[1], (uint32_t)(i & 1))) break;
-        if (more) issue_s(1, nbuf);
-        issue_pv(1, buf, i > 0);
+        issue_pv(1, buf, sb, i > 0);
         // both PVs of this key tile have read its operands: buffer free
         if (elect_one()) {
           umma_commit(&pv_done[1]);
           umma_commit(&kv_empty[buf]);
         }
         __syncwarp();
+        if (i + 2 < ntl) {
+          const int nb2 = (i + 2) % NB;
+          if (!wait(&kv_full[nb2], (uint32_t)(((i + 2) / NB) & 1))) break;
+          if (!wait(&pv_done[0], (uint32_t)(i & 1))) break;
+          issue_s(0, nb2, sb);
+          if (!wait(&pv_done[1], (uint32_t)(i & 1))) break;
+          issue_s(1, nb2, sb);
+        }
       }
     }
     // everything issued completes before the epilogue and the exit
@@ -475,8 +489,6 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     const int loA = (a.window > 0) ? max(0, pA + 1 - a.window) : 0;
     const float fA = rowf[R];
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t tS = trow + C::SCOL + 64 * j;
-    const uint32_t tP = trow + C::PCOL + 64 * j;
     const uint32_t tO = trow + C::OCOL + D * j;
     // positions of this query tile's first and last rows: a key tile inside
     // [last row's window start, first row] is visible to every row
@@ -493,7 +505,10 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     bool ok = true;
     for (int i = 0; i < ntl; ++i) {
       const int buf = i % NB, t = t0 + i;
-      const bool w = __all_sync(0xffffffffu, mbar_wait(&s_full[j], (uint32_t)(i & 1)));
+      // S of this tile in S/P' buffer i & 1 (its P' replaces it there)
+      const int sb = i & 1;
+      const uint32_t tS = trow + 64 * (2 * j + sb), tP = tS;
+      const bool w = __all_sync(0xffffffffu, mbar_wait(&s_full[2 * j + sb], (uint32_t)((i >> 1) & 1)));
       if (!w && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
       if (!w || __any_sync(0xffffffffu, *s_abort)) { ok = false; break; }
       tc_fence_after();
@@ -560,15 +575,15 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       // l and O both carry the range factor 2^(WKP - vexp) (64 for static
       // scales), so both follow the max and the V-scale exponent
       l *= al;
-      // the previous PV has read P'_j and updated O_j
-      if (i > 0) {
+      // O holds data from the first PV on; it is rescaled (rarely) once the
+      // previous PV has updated it.  P' needs no wait: its buffer held this
+      // tile's S, and the PV that last read P' there completed before that S
+      // was issued.
+      if (i > 0 && __any_sync(0xffffffffu, al != 1.f)) {
         const bool w2 = __all_sync(0xffffffffu, mbar_wait(&pv_done[j], (uint32_t)((i - 1) & 1)));
         if (!w2 && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
         if (!w2 || __any_sync(0xffffffffu, *s_abort)) { ok = false; break; }
         tc_fence_after();
-      }
-      // O holds data from the first PV on
-      if (i > 0 && __any_sync(0xffffffffu, al != 1.f)) {
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           float v[32];
