@@ -78,7 +78,9 @@ struct WCfg {
   static constexpr int KB = WKT * D * 2;                    // one K buffer: D/64 blocks of 64 x 128 B
   static constexpr int VTB = D * WKT * 2;                   // one V^T buffer: D rows of 128 B
   static constexpr int LDV = (D + 8) * 2;                   // row pitch of the V staging copy
-  static constexpr int STG = (WKT * LDV + 1023) / 1024 * 1024;
+  // V staging copy (INT4 only: FP8 codes are transposed straight from the
+  // raw tile)
+  static constexpr int STG = (MODE == INT4_PER_TOKEN_HEAD) ? (WKT * LDV + 1023) / 1024 * 1024 : 0;
   // one scale buffer: K scales, V scales, then ints: V-scale exponent of
   // each 32-key half, whether every page tile was fetched
   static constexpr int SCS = 2 * WKT * 4 + 16;
@@ -306,37 +308,90 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       const unsigned have = (unsigned)s_have[st];
       const uint8_t* base = raw + st * C::RAWS;
       uint8_t* kb = k16 + buf * C::KB;
-      // K into kb, V into the row-major staging copy (zeros where nothing was
-      // fetched or the position lies outside [kmin, pmax]).  Each thread takes
-      // NIT chunks of K and as many of V; all loads first, then conversions.
+      // K into kb (and, for INT4, V into the row-major staging copy); zeros
+      // where nothing was fetched or the position lies outside [kmin, pmax].
+      // Each thread takes NIT chunks; all loads first, then conversions.
+      constexpr bool VSTG = (MODE == INT4_PER_TOKEN_HEAD);
       constexpr int NIT = WKT * CPR / (WS_CONV * 32);
       static_assert(NIT * WS_CONV * 32 == WKT * CPR, "chunks per converter thread");
-      uint4 wk[NIT], wv[NIT];
+      {
+        uint4 wk[NIT], wv[NIT];
 #pragma unroll
-      for (int it = 0; it < NIT; ++it) {
-        const int cc = ct_ + it * WS_CONV * 32;
-        const int key = cc / CPR, ch = cc % CPR;
-        const int sub = key >> 4, kr = key & 15;
-        const int pos = t * WKT + key;
-        const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
-        const uint32_t off = swz((uint32_t)(kr * C::RB + ch * 16));
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        wk[it] = live ? *reinterpret_cast<const uint4*>(base + sub * C::TBP + off) : z;
-        wv[it] = live ? *reinterpret_cast<const uint4*>(base + (SUB + sub) * C::TBP + off) : z;
+        for (int it = 0; it < NIT; ++it) {
+          const int cc = ct_ + it * WS_CONV * 32;
+          const int key = cc / CPR, ch = cc % CPR;
+          const int sub = key >> 4, kr = key & 15;
+          const int pos = t * WKT + key;
+          const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
+          const uint32_t off = swz((uint32_t)(kr * C::RB + ch * 16));
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          wk[it] = live ? *reinterpret_cast<const uint4*>(base + sub * C::TBP + off) : z;
+          if constexpr (VSTG)
+            wv[it] = live ? *reinterpret_cast<const uint4*>(base + (SUB + sub) * C::TBP + off) : z;
+        }
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+          const int cc = ct_ + it * WS_CONV * 32;
+          const int key = cc / CPR, ch = cc % CPR;
+          const int d0 = ch * EPC;
+          uint4 ok_[4], ov[4];
+          convert16<MODE>(wk[it], ok_);
+          if constexpr (VSTG) convert16<MODE>(wv[it], ov);
+#pragma unroll
+          for (int qq = 0; qq < EPC / 8; ++qq) {
+            const int d = d0 + 8 * qq;
+            *reinterpret_cast<uint4*>(kb + (d >> 6) * (WKT * 128) + swc(key, (d & 63) >> 3)) = ok_[qq];
+            if constexpr (VSTG) *reinterpret_cast<uint4*>(stg + key * C::LDV + d * 2) = ov[qq];
+          }
+        }
       }
+      uint8_t* vb = vt16 + buf * C::VTB;
+      if constexpr (!VSTG) {
+        // V^T straight from the raw FP8 codes: a task is 8 keys x 4 d.  Its
+        // 8 words (one per key: codes of d..d+3) are transposed in registers
+        // into 4 rows of 8 codes each, converted, and stored as one 16-byte
+        // chunk per d row.  Lane-to-task map: consecutive lanes take
+        // consecutive d groups, and the key group turns with the lane pair and
+        // the warp, so the 4-byte loads and the 16-byte stores of a warp meet
+        // no bank twice.
+        constexpr int DG = D / 4;                   // d groups of 4
+        constexpr int NT = 8 * DG / (WS_CONV * 32); // tasks per thread (2 at D 128, 1 at D 64)
+        static_assert(NT * WS_CONV * 32 == 8 * DG, "V^T tasks per converter thread");
+        const int cw = warp - WS_SOFT;              // converter warp 0..3
+        const int dg = lane % DG, hs = lane / DG;
 #pragma unroll
-      for (int it = 0; it < NIT; ++it) {
-        const int cc = ct_ + it * WS_CONV * 32;
-        const int key = cc / CPR, ch = cc % CPR;
-        const int d0 = ch * EPC;
-        uint4 ok_[4], ov[4];
-        convert16<MODE>(wk[it], ok_);
-        convert16<MODE>(wv[it], ov);
+        for (int it = 0; it < NT; ++it) {
+          const int kg = (((dg >> 1) + cw) & 3) + 4 * (it + hs);
+          uint32_t x[8];
 #pragma unroll
-        for (int qq = 0; qq < EPC / 8; ++qq) {
-          const int d = d0 + 8 * qq;
-          *reinterpret_cast<uint4*>(kb + (d >> 6) * (WKT * 128) + swc(key, (d & 63) >> 3)) = ok_[qq];
-          *reinterpret_cast<uint4*>(stg + key * C::LDV + d * 2) = ov[qq];
+          for (int k = 0; k < 8; ++k) {
+            const int key = 8 * kg + k;
+            const int sub = key >> 4, kr = key & 15;
+            const int pos = t * WKT + key;
+            const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
+            x[k] = live ? *reinterpret_cast<const uint32_t*>(base + (SUB + sub) * C::TBP +
+                                                            swz((uint32_t)(kr * C::RB + 4 * dg)))
+                        : 0u;
+          }
+          uint32_t lo[4], hi[4];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t* y = x + 4 * half;
+            const uint32_t t0 = __byte_perm(y[0], y[1], 0x5140), t1 = __byte_perm(y[0], y[1], 0x7362);
+            const uint32_t t2 = __byte_perm(y[2], y[3], 0x5140), t3 = __byte_perm(y[2], y[3], 0x7362);
+            uint32_t* o = half ? hi : lo;
+            o[0] = __byte_perm(t0, t2, 0x5410);     // byte dd of keys 0..3 (or 4..7)
+            o[1] = __byte_perm(t0, t2, 0x7632);
+            o[2] = __byte_perm(t1, t3, 0x5410);
+            o[3] = __byte_perm(t1, t3, 0x7632);
+          }
+#pragma unroll
+          for (int dd = 0; dd < 4; ++dd) {
+            uint4 v;
+            e4m3x4_f16(lo[dd], v.x, v.y);
+            e4m3x4_f16(hi[dd], v.z, v.w);
+            *reinterpret_cast<uint4*>(vb + swc(4 * dg + dd, kg)) = v;
+          }
         }
       }
       {
@@ -361,36 +416,40 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
         }
         if (ct_ == 0) tinfo[2] = (have == (1u << SUB) - 1u) ? 1 : 0;
       }
-      named_sync(CONV_BAR, WS_CONV * 32);
-      // the raw stage has been read
-      if (ct_ == 0) mbar_arrive(&raw_empty[st]);
-      // V^T: rows d, chunks of 8 keys, from the staging copy
-      uint8_t* vb = vt16 + buf * C::VTB;
-      constexpr int NVT = (WKT / 8) * (D / 2) / (WS_CONV * 32);
-      static_assert(NVT * WS_CONV * 32 == (WKT / 8) * (D / 2), "V^T tasks per converter thread");
+      if constexpr (VSTG) {
+        named_sync(CONV_BAR, WS_CONV * 32);
+        // the raw stage has been read
+        if (ct_ == 0) mbar_arrive(&raw_empty[st]);
+        // V^T: rows d, chunks of 8 keys, from the staging copy
+        constexpr int NVT = (WKT / 8) * (D / 2) / (WS_CONV * 32);
+        static_assert(NVT * WS_CONV * 32 == (WKT / 8) * (D / 2), "V^T tasks per converter thread");
 #pragma unroll
-      for (int it = 0; it < NVT; ++it) {
-        const int u = ct_ + it * WS_CONV * 32;
-        const int dp = u % (D / 2), kg = u / (D / 2);
-        uint32_t wv[8];
+        for (int it = 0; it < NVT; ++it) {
+          const int u = ct_ + it * WS_CONV * 32;
+          const int dp = u % (D / 2), kg = u / (D / 2);
+          uint32_t wv[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          wv[k] = *reinterpret_cast<const uint32_t*>(stg + (8 * kg + k) * C::LDV + dp * 4);
-        uint4 e, f;
-        e.x = __byte_perm(wv[0], wv[1], 0x5410);
-        e.y = __byte_perm(wv[2], wv[3], 0x5410);
-        e.z = __byte_perm(wv[4], wv[5], 0x5410);
-        e.w = __byte_perm(wv[6], wv[7], 0x5410);
-        f.x = __byte_perm(wv[0], wv[1], 0x7632);
-        f.y = __byte_perm(wv[2], wv[3], 0x7632);
-        f.z = __byte_perm(wv[4], wv[5], 0x7632);
-        f.w = __byte_perm(wv[6], wv[7], 0x7632);
-        *reinterpret_cast<uint4*>(vb + swc(2 * dp, kg)) = e;
-        *reinterpret_cast<uint4*>(vb + swc(2 * dp + 1, kg)) = f;
+          for (int k = 0; k < 8; ++k)
+            wv[k] = *reinterpret_cast<const uint32_t*>(stg + (8 * kg + k) * C::LDV + dp * 4);
+          uint4 e, f;
+          e.x = __byte_perm(wv[0], wv[1], 0x5410);
+          e.y = __byte_perm(wv[2], wv[3], 0x5410);
+          e.z = __byte_perm(wv[4], wv[5], 0x5410);
+          e.w = __byte_perm(wv[6], wv[7], 0x5410);
+          f.x = __byte_perm(wv[0], wv[1], 0x7632);
+          f.y = __byte_perm(wv[2], wv[3], 0x7632);
+          f.z = __byte_perm(wv[4], wv[5], 0x7632);
+          f.w = __byte_perm(wv[6], wv[7], 0x7632);
+          *reinterpret_cast<uint4*>(vb + swc(2 * dp, kg)) = e;
+          *reinterpret_cast<uint4*>(vb + swc(2 * dp + 1, kg)) = f;
+        }
       }
       fence_proxy_async();
       named_sync(CONV_BAR, WS_CONV * 32);
-      if (ct_ == 0) mbar_arrive(&kv_full[buf]);
+      if (ct_ == 0) {
+        if constexpr (!VSTG) mbar_arrive(&raw_empty[st]);   // the raw stage has been read
+        mbar_arrive(&kv_full[buf]);
+      }
     }
   } else if (warp == WS_MMA) {
     // ---- MMA issuer: one elected lane issues and commits (elect.sync picks
