@@ -16,9 +16,9 @@
 //    stages; lane s takes page tile s.
 //  * warps 8-11, converters: raw codes -> f16 in the tensor cores' layout,
 //    K as 64 rows of D (K-major, 128-byte swizzle) and V transposed (D rows
-//    of 64 keys) through a row-major staging copy; K and V scales (zero for a
+//    of 64 keys, by a byte transpose in registers); K and V scales (zero for a
 //    key outside the CTA's range or on a page that was not fetched) and the
-//    tile's largest V-scale exponent.  Two operand buffers.
+//    tile's largest V-scale exponent.  Three operand buffers.
 //  * warp 13, MMA issuer (one thread): S_j = Q_j K^T (M 128, N 64) into
 //    tensor memory for each query tile j, and O_j += P'_j V with P'_j read
 //    from tensor memory, every term of its f16 hi + lo split.  Each query
@@ -77,10 +77,6 @@ struct WCfg {
   static constexpr int QB = WROWS * D * 2;                  // one query tile: D/64 blocks of 128 x 128 B
   static constexpr int KB = WKT * D * 2;                    // one K buffer: D/64 blocks of 64 x 128 B
   static constexpr int VTB = D * WKT * 2;                   // one V^T buffer: D rows of 128 B
-  static constexpr int LDV = (D + 8) * 2;                   // row pitch of the V staging copy
-  // V staging copy (INT4 only: FP8 codes are transposed straight from the
-  // raw tile)
-  static constexpr int STG = (MODE == INT4_PER_TOKEN_HEAD) ? (WKT * LDV + 1023) / 1024 * 1024 : 0;
   // one scale buffer: K scales, V scales, then ints: V-scale exponent of
   // each 32-key half, whether every page tile was fetched
   static constexpr int SCS = 2 * WKT * 4 + 16;
@@ -88,7 +84,7 @@ struct WCfg {
   static constexpr int BARB = 32 * 8;                       // barriers
   static constexpr int LIMIT = 232448 - 1024;               // per-CTA shared memory, minus slack
   // operand buffers (K, V^T, scales): three when they fit beside two raw stages
-  static constexpr int fixed_of(int nb) { return 2 * QB + nb * (KB + VTB + SCS) + STG + ROWB + BARB + 64; }
+  static constexpr int fixed_of(int nb) { return 2 * QB + nb * (KB + VTB + SCS) + ROWB + BARB + 64; }
   static constexpr int NB = (fixed_of(3) + 2 * RAWS <= LIMIT) ? 3 : 2;
   static constexpr int FIXED = fixed_of(NB);
   static constexpr int NR = (FIXED + 4 * RAWS <= LIMIT) ? 4 : ((FIXED + 3 * RAWS <= LIMIT) ? 3 : 2);
@@ -122,8 +118,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   uint8_t* q16 = raw + NR * C::RAWS;                         // 2 query tiles
   uint8_t* k16 = q16 + 2 * C::QB;                            // NB K buffers
   uint8_t* vt16 = k16 + NB * C::KB;                          // NB V^T buffers
-  uint8_t* stg = vt16 + NB * C::VTB;                         // V staging copy
-  uint8_t* scb = stg + C::STG;                               // NB scale buffers
+  uint8_t* scb = vt16 + NB * C::VTB;                         // NB scale buffers
   float* rowf = reinterpret_cast<float*>(scb + NB * C::SCS); // [2][128] score factor per row
   int* rowp = reinterpret_cast<int*>(rowf + 2 * WROWS);      // [2][128] position (-1: no row)
   uint64_t* bars = reinterpret_cast<uint64_t*>(rowp + 2 * WROWS);
@@ -132,8 +127,12 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   uint64_t* kv_full = raw_empty + NR;                        // [NB] converters -> MMA
   uint64_t* kv_empty = kv_full + NB;                         // [NB] MMA (commit) -> converters
   uint64_t* s_full = kv_empty + NB;                          // [2][2] MMA (commit) -> softmax j, per S buffer
-  uint64_t* p_full = s_full + 4;                             // [2] softmax j (128 arrivals) -> MMA
-  uint64_t* pv_done = p_full + 2;                            // [2] MMA (commit) -> softmax j
+  // P' of query tile j in S/P' buffer b: [2][2], 128 arrivals each.  One
+  // barrier per buffer: a softmax warpgroup may finish key tile t + 1 before
+  // the MMA issuer waits for its tile t, and a barrier per query tile would
+  // then complete two phases ahead of its waiter.
+  uint64_t* p_full = s_full + 4;
+  uint64_t* pv_done = p_full + 4;                            // [2] MMA (commit) -> softmax j
   uint64_t* o_fin = pv_done + 2;                             // MMA (commit) -> softmax, at the end
   int* s_have = reinterpret_cast<int*>(bars + 32);           // [NR] fetched page tiles per stage
   volatile int* s_abort = s_have + 4;
@@ -171,11 +170,11 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int s = 0; s < 4; ++s) mbar_init(&s_full[s], 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 4 * 32);
-      mbar_init(&pv_done[s], 1);
     }
+    for (int s = 0; s < 2; ++s) mbar_init(&pv_done[s], 1);
     mbar_init(o_fin, 1);
     mbar_init_fence();
     *s_abort = 0;
@@ -308,14 +307,13 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       const unsigned have = (unsigned)s_have[st];
       const uint8_t* base = raw + st * C::RAWS;
       uint8_t* kb = k16 + buf * C::KB;
-      // K into kb (and, for INT4, V into the row-major staging copy); zeros
-      // where nothing was fetched or the position lies outside [kmin, pmax].
-      // Each thread takes NIT chunks; all loads first, then conversions.
-      constexpr bool VSTG = (MODE == INT4_PER_TOKEN_HEAD);
+      // K into kb; zeros where nothing was fetched or the position lies
+      // outside [kmin, pmax].  Each thread takes NIT chunks; all loads first,
+      // then conversions.
       constexpr int NIT = WKT * CPR / (WS_CONV * 32);
       static_assert(NIT * WS_CONV * 32 == WKT * CPR, "chunks per converter thread");
       {
-        uint4 wk[NIT], wv[NIT];
+        uint4 wk[NIT];
 #pragma unroll
         for (int it = 0; it < NIT; ++it) {
           const int cc = ct_ + it * WS_CONV * 32;
@@ -324,29 +322,25 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
           const int pos = t * WKT + key;
           const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
           const uint32_t off = swz((uint32_t)(kr * C::RB + ch * 16));
-          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-          wk[it] = live ? *reinterpret_cast<const uint4*>(base + sub * C::TBP + off) : z;
-          if constexpr (VSTG)
-            wv[it] = live ? *reinterpret_cast<const uint4*>(base + (SUB + sub) * C::TBP + off) : z;
+          wk[it] = live ? *reinterpret_cast<const uint4*>(base + sub * C::TBP + off)
+                        : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int it = 0; it < NIT; ++it) {
           const int cc = ct_ + it * WS_CONV * 32;
           const int key = cc / CPR, ch = cc % CPR;
           const int d0 = ch * EPC;
-          uint4 ok_[4], ov[4];
+          uint4 ok_[4];
           convert16<MODE>(wk[it], ok_);
-          if constexpr (VSTG) convert16<MODE>(wv[it], ov);
 #pragma unroll
           for (int qq = 0; qq < EPC / 8; ++qq) {
             const int d = d0 + 8 * qq;
             *reinterpret_cast<uint4*>(kb + (d >> 6) * (WKT * 128) + swc(key, (d & 63) >> 3)) = ok_[qq];
-            if constexpr (VSTG) *reinterpret_cast<uint4*>(stg + key * C::LDV + d * 2) = ov[qq];
           }
         }
       }
       uint8_t* vb = vt16 + buf * C::VTB;
-      if constexpr (!VSTG) {
+      if constexpr (MODE != INT4_PER_TOKEN_HEAD) {
         // V^T straight from the raw FP8 codes: a task is 8 keys x 4 d.  Its
         // 8 words (one per key: codes of d..d+3) are transposed in registers
         // into 4 rows of 8 codes each, converted, and stored as one 16-byte
@@ -394,6 +388,63 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
           }
         }
       }
+      if constexpr (MODE == INT4_PER_TOKEN_HEAD) {
+        // V^T straight from the raw INT4 codes: a task is 8 keys x 4 bytes
+        // (8 d).  The 8 words are transposed as for FP8; byte bb of 4 keys
+        // then gives the f16 values of d = 2bb (low nibbles) and 2bb + 1 (high
+        // nibbles, read 16x and scaled back exactly).
+        constexpr int BG = D / 8;                   // 4-byte groups of a key row
+        const int cw = warp - WS_SOFT;
+        int bg, kg;
+        if constexpr (BG >= 16) {                   // 128 tasks, one per thread
+          bg = lane % BG;
+          kg = (((bg >> 1) + cw) & 3) + 4 * (lane / BG);
+        } else {                                    // 64 tasks: the first 64 threads
+          bg = ct_ % BG;
+          kg = ct_ / BG;
+        }
+        if (kg < 8) {
+          uint32_t x[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int key = 8 * kg + k;
+            const int sub = key >> 4, kr = key & 15;
+            const int pos = t * WKT + key;
+            const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
+            x[k] = live ? *reinterpret_cast<const uint32_t*>(base + (SUB + sub) * C::TBP +
+                                                            swz((uint32_t)(kr * C::RB + 4 * bg)))
+                        : 0u;
+          }
+          uint32_t lo[4], hi[4];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t* y = x + 4 * half;
+            const uint32_t t0 = __byte_perm(y[0], y[1], 0x5140), t1 = __byte_perm(y[0], y[1], 0x7362);
+            const uint32_t t2 = __byte_perm(y[2], y[3], 0x5140), t3 = __byte_perm(y[2], y[3], 0x7362);
+            uint32_t* o = half ? hi : lo;
+            o[0] = __byte_perm(t0, t2, 0x5410);
+            o[1] = __byte_perm(t0, t2, 0x7632);
+            o[2] = __byte_perm(t1, t3, 0x5410);
+            o[3] = __byte_perm(t1, t3, 0x7632);
+          }
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            uint32_t ev[4], od[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              // keys 2q, 2q + 1: bytes (q & 1) * 2 and +1 of lo or hi
+              const uint32_t wq = (q < 2) ? lo[bb] : hi[bb];
+              const uint32_t pr = __byte_perm(wq, 0u, (q & 1) ? 0x7372 : 0x7170);
+              ev[q] = nib2_f16x2<0>(pr);
+              const uint32_t h16 = nib2_f16x2<1>(pr);
+              asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(od[q]) : "r"(h16), "r"(0x2C002C00u));   // x 1/16
+            }
+            const int d = 8 * bg + 2 * bb;
+            *reinterpret_cast<uint4*>(vb + swc(d, kg)) = make_uint4(ev[0], ev[1], ev[2], ev[3]);
+            *reinterpret_cast<uint4*>(vb + swc(d + 1, kg)) = make_uint4(od[0], od[1], od[2], od[3]);
+          }
+        }
+      }
       {
         // scales: threads 0..63 K, 64..127 V (scale 0: no key)
         float* ksm = reinterpret_cast<float*>(scb + buf * C::SCS);
@@ -416,38 +467,10 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
         }
         if (ct_ == 0) tinfo[2] = (have == (1u << SUB) - 1u) ? 1 : 0;
       }
-      if constexpr (VSTG) {
-        named_sync(CONV_BAR, WS_CONV * 32);
-        // the raw stage has been read
-        if (ct_ == 0) mbar_arrive(&raw_empty[st]);
-        // V^T: rows d, chunks of 8 keys, from the staging copy
-        constexpr int NVT = (WKT / 8) * (D / 2) / (WS_CONV * 32);
-        static_assert(NVT * WS_CONV * 32 == (WKT / 8) * (D / 2), "V^T tasks per converter thread");
-#pragma unroll
-        for (int it = 0; it < NVT; ++it) {
-          const int u = ct_ + it * WS_CONV * 32;
-          const int dp = u % (D / 2), kg = u / (D / 2);
-          uint32_t wv[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            wv[k] = *reinterpret_cast<const uint32_t*>(stg + (8 * kg + k) * C::LDV + dp * 4);
-          uint4 e, f;
-          e.x = __byte_perm(wv[0], wv[1], 0x5410);
-          e.y = __byte_perm(wv[2], wv[3], 0x5410);
-          e.z = __byte_perm(wv[4], wv[5], 0x5410);
-          e.w = __byte_perm(wv[6], wv[7], 0x5410);
-          f.x = __byte_perm(wv[0], wv[1], 0x7632);
-          f.y = __byte_perm(wv[2], wv[3], 0x7632);
-          f.z = __byte_perm(wv[4], wv[5], 0x7632);
-          f.w = __byte_perm(wv[6], wv[7], 0x7632);
-          *reinterpret_cast<uint4*>(vb + swc(2 * dp, kg)) = e;
-          *reinterpret_cast<uint4*>(vb + swc(2 * dp + 1, kg)) = f;
-        }
-      }
       fence_proxy_async();
       named_sync(CONV_BAR, WS_CONV * 32);
       if (ct_ == 0) {
-        if constexpr (!VSTG) mbar_arrive(&raw_empty[st]);   // the raw stage has been read
+        mbar_arrive(&raw_empty[st]);                // the raw stage has been read
         mbar_arrive(&kv_full[buf]);
       }
     }
@@ -513,11 +536,11 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       }
       for (int i = 0; go && i < ntl; ++i) {
         const int buf = i % NB, sb = i & 1;
-        if (!wait(&p_full[0], (uint32_t)(i & 1))) break;
+        if (!wait(&p_full[sb], (uint32_t)((i >> 1) & 1))) break;
         issue_pv(0, buf, sb, i > 0);
         if (elect_one()) umma_commit(&pv_done[0]);
         __syncwarp();
-        if (!wait(&p_full[1], (uint32_t)(i & 1))) break;
+        if (!wait(&p_full[2 + sb], (uint32_t)((i >> 1) & 1))) break;
         issue_pv(1, buf, sb, i > 0);
         // both PVs of this key tile have read its operands: buffer free
         if (elect_one()) {
@@ -686,7 +709,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[j]);
+      mbar_arrive(&p_full[2 * j + sb]);
     }
     // ---- epilogue: out = O x unscale / l (rows without a query store nothing)
     const bool fin = __all_sync(0xffffffffu, mbar_wait(o_fin, 0u));
