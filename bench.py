@@ -9,11 +9,13 @@ scales, q, out, block table, new K/V and slots) per second.  The same run
 also times a prefill-shaped cache write of the whole 1,048,576-token context
 (cache-write GB/s), and then measures every other workload and mode the same
 way (the "configs" block: decode and fill GB/s and their fractions of the
-measured HBM peak, per-kernel CUDA-event times).
+measured HBM peak, per-kernel CUDA-event times) and a few prefill chunks (the
+"prefill" block: TFLOP/s against the tensor peak).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--mode fp8_per_token_head]
                     [--workload llama70b_128k|llama8b|gptoss20b|gemma_d256]
                     [--skip-sliding] [--workers N] [--graph | --no-graph] [--no-configs]
+                    [--no-prefill]
                     [--batch B] [--context L] [--layer I]     # smaller cases (profiling)
     python bench.py --impl reference     # the CPU oracle on a bounded sample
     python bench.py --prefill --workload llama8b|gemma_d256     # prefill TFLOP/s
@@ -565,6 +567,8 @@ def run_gpu(args):
     torch.cuda.empty_cache()
     if world == 1 and not args.no_configs:
         res["configs"] = config_block(args, dev)
+    if world == 1 and not args.no_prefill:
+        res["prefill"] = prefill_block(args)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args, kvq.MODE_NAMES[args.mode])
     if dist is not None:
@@ -674,6 +678,29 @@ def measure_config(args, dev, workload: str, mode: str, skip: bool, steps: int =
 
 def config_block(args, dev) -> list:
     return [measure_config(args, dev, wname, mode, skip) for wname, mode, skip in CONFIG_BLOCK]
+
+
+# Prefill chunks timed after the decode configurations (kvq_prefill_attention;
+# TFLOP/s against the tensor peak), so the default run records the prefill
+# kernels too: (workload, mode).
+PREFILL_BLOCK = [
+    ("llama8b", "fp8_per_token_head"),
+    ("llama8b", "fp8_per_head"),
+    ("llama8b", "int4_per_token_head"),
+    ("gemma_d256", "fp8_per_token_head"),
+]
+
+
+def prefill_block(args) -> list:
+    out = []
+    for wname, mode in PREFILL_BLOCK:
+        sub = argparse.Namespace(workload=wname, mode=mode, steps=5, warmup=3)
+        r = run_prefill(sub)
+        out.append({"workload": wname, "mode": mode, "chunk": r["config"]["workload"],
+                    "kernel": r["roofline"]["kernel"], "tflops": r["value"],
+                    "frac_of_peak": r["roofline"]["frac"], "ms": r["ms_per_step"],
+                    "tokens_per_s": r["config"]["tokens_per_s"]})
+    return out
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -1028,6 +1055,8 @@ def main(argv=None):
                     help="run only this layer of the workload (its window and mode)")
     ap.add_argument("--cpu-seqs", type=int, default=0, help="0: the workload's default sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill chunks timed after the decode configurations")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the block that measures every workload and mode after the headline")
     ap.add_argument("--latency-sweep", action="store_true",
