@@ -123,3 +123,30 @@ def test_chunk_longer_than_context_is_reported():
     kvq.kvq_prefill_attention(r.ctx, 0, q, r.kc, r.vc, r.pg.block_table, qs, r.pg.context_lens,
                               out, max_query_len=38, k_cache_scale=r.ks, v_cache_scale=r.vs)
     assert kvq.kvq_get_device_error() == kvq.STATUS.index("KVQ_ERR_BAD_INDEX")
+
+
+@pytest.mark.parametrize("name,mode", [("llama8b", orc.FP8_PER_TOKEN_HEAD),
+                                       ("llama8b", orc.INT4_PER_TOKEN_HEAD),
+                                       ("llama8b", orc.BF16),
+                                       ("gemma", orc.FP8_PER_TOKEN_HEAD)])
+def test_bad_block_id_is_reported_and_masked(name, mode):
+    """A block id past the cache in the middle of a sequence's table row: the
+    prefill kernels fetch nothing for that page, report BAD_INDEX, and treat
+    its positions as masked, so every output stays finite."""
+    w, chunks = CASES[name]
+    r = LayerRun(w, mode, layer=w.num_layers - 1)
+    r.write()
+    kvq = K()
+    b = 1
+    bt = r.pg.block_table.clone()
+    bt[b, 3] = r.pg.num_blocks + 5
+    T = sum(chunks)
+    q = _queries(w, T, 17)
+    qs = torch.tensor(np.concatenate([[0], np.cumsum(chunks)]), dtype=torch.int32, device="cuda")
+    out = torch.full((T, w.Hq, w.D), float("nan"), dtype=torch.float32, device="cuda")
+    kvq.kvq_prefill_attention(r.ctx, r.layer, q, r.kc, r.vc, bt, qs, r.pg.context_lens, out,
+                              max_query_len=max(chunks), k_scale=r.k_scale, v_scale=r.v_scale,
+                              k_cache_scale=r.ks, v_cache_scale=r.vs)
+    torch.cuda.synchronize()
+    assert kvq.kvq_get_device_error() == kvq.STATUS.index("KVQ_ERR_BAD_INDEX")
+    assert torch.isfinite(out).all()
