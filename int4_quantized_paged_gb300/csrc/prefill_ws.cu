@@ -29,8 +29,8 @@
 //    tensor cores work on one query tile while the other's softmax runs.
 //  * warps 0-3 and 4-7, softmax of query tile 0 and 1: one thread per row
 //    (its tensor-memory lane) loads the row's 64 scores, applies the K scale
-//    and masks, keeps a lazily moved reference max (moved only when a tile
-//    exceeds it by more than 2^8), rescales the row of O in tensor memory
+//    and masks, keeps a lazily moved reference max (moved only when a tile's
+//    max exceeds it by more than 8 in log2 units), rescales the row of O in tensor memory
 //    when it moves, and stores P' = p x v_scale x 2^k (f16 hi + lo) over the
 //    scores it has read.
 // Tensor memory: two S/P' buffers per query tile (64 columns each), O_0, O_1
