@@ -52,12 +52,20 @@
 namespace kvq {
 namespace {
 
-constexpr int WS_SOFT = 8;                          // softmax warps (two warpgroups)
 constexpr int WS_CONV = 4;                          // converter warps
-constexpr int WS_PROD = WS_SOFT + WS_CONV;          // producer warp
-constexpr int WS_MMA = WS_PROD + 1;                 // MMA-issuing warp
-constexpr int WS_THREADS = (WS_MMA + 1) * 32;       // 448
 constexpr int WROWS = 128;                          // rows per query tile (the MMA's M)
+
+// Warp roles: NQ query tiles per CTA (two at head_dim 64 and 128; one at 256,
+// whose O needs 256 tensor-memory columns), a softmax warpgroup per query
+// tile, then the converters, the producer and the MMA issuer.
+template <int D>
+struct WRoles {
+  static constexpr int NQ = (D == 256) ? 1 : 2;
+  static constexpr int SOFT = 4 * NQ;                // softmax warps
+  static constexpr int PROD = SOFT + WS_CONV;        // producer warp
+  static constexpr int MMA = PROD + 1;               // MMA-issuing warp
+  static constexpr int THREADS = (MMA + 1) * 32;     // 448 or 320
+};
 constexpr int WKT = 64;                             // keys per tile
 constexpr int WKP = 6;                              // P' = p v_scale 2^(WKP - vexp) < 2^15 (p <= 2^8)
 constexpr float WLAZY = 8.f;                        // the reference max moves when exceeded by this
@@ -74,7 +82,11 @@ struct WCfg {
   static constexpr int RAW = 2 * SUB * TBP;                 // K and V page tiles of a key tile
   static constexpr int SCB = DYN ? 2 * SUB * 64 : 0;        // their K and V scales
   static constexpr int RAWS = (RAW + SCB + 1023) / 1024 * 1024;
+  static constexpr int NQ = WRoles<D>::NQ;
   static constexpr int QB = WROWS * D * 2;                  // one query tile: D/64 blocks of 128 x 128 B
+  // queries in shared memory (two query tiles); with one query tile (D 256)
+  // they live in tensor memory instead, the A operand of S
+  static constexpr int QSM = (NQ == 2) ? 2 * QB : 0;
   static constexpr int KB = WKT * D * 2;                    // one K buffer: D/64 blocks of 64 x 128 B
   static constexpr int VTB = D * WKT * 2;                   // one V^T buffer: D rows of 128 B
   // one scale buffer: K scales, V scales, then ints: V-scale exponent of
@@ -84,25 +96,31 @@ struct WCfg {
   static constexpr int BARB = 32 * 8;                       // barriers
   static constexpr int LIMIT = 232448 - 1024;               // per-CTA shared memory, minus slack
   // operand buffers (K, V^T, scales): three when they fit beside two raw stages
-  static constexpr int fixed_of(int nb) { return 2 * QB + nb * (KB + VTB + SCS) + ROWB + BARB + 64; }
+  static constexpr int fixed_of(int nb) { return QSM + nb * (KB + VTB + SCS) + ROWB + BARB + 64; }
   static constexpr int NB = (fixed_of(3) + 2 * RAWS <= LIMIT) ? 3 : 2;
   static constexpr int FIXED = fixed_of(NB);
   static constexpr int NR = (FIXED + 4 * RAWS <= LIMIT) ? 4 : ((FIXED + 3 * RAWS <= LIMIT) ? 3 : 2);
   static constexpr int SMEM = NR * RAWS + FIXED + 1024;
-  // tensor-memory columns
-  // S/P' buffer b of query tile j at 64 (2 j + b): S (fp32, 64 columns),
-  // then P' (f16 hi in the first 32 columns, lo in the next 32) in its place
-  static constexpr int OCOL = 256;                          // O_j at 256 + D j
+  // Tensor-memory columns.  S/P' buffer b of query tile j: S (fp32, 64
+  // columns), then P' (f16 hi in the first 32 columns, lo in the next 32) in
+  // its place.  Two query tiles: S/P' at 64 (2 j + b), O_j at 256 + D j.  One
+  // query tile (D 256): O at 0, S/P' at 256 + 64 b, Q (f16, D / 2 columns) at
+  // 384.
+  __host__ __device__ static constexpr int scol(int j, int b) { return NQ == 2 ? 64 * (2 * j + b) : 256 + 64 * b; }
+  __host__ __device__ static constexpr int ocol(int j) { return NQ == 2 ? 256 + D * j : 0; }
+  static constexpr int QCOL = 384;
   static constexpr int TCOLS = 512;
-  static_assert(OCOL + 2 * D <= TCOLS, "tensor memory");
+  static_assert(NQ == 2 ? 256 + 2 * D <= TCOLS : QCOL + D / 2 <= TCOLS, "tensor memory");
   static_assert(SMEM <= 232448, "shared memory");
 };
 
 template <int MODE, int D, int G>
-__global__ void __launch_bounds__(WS_THREADS, 1)
+__global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
     prefill_ws_kernel(const PrefillArgs pa, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap) {
   using C = WCfg<MODE, D>;
+  using RL = WRoles<D>;
+  constexpr int NQ = RL::NQ;
   const DecodeArgs& a = pa.d;
   constexpr int SUB = C::SUB;
   constexpr int NR = C::NR;
@@ -115,8 +133,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* raw = smem;                                       // NR stages
-  uint8_t* q16 = raw + NR * C::RAWS;                         // 2 query tiles
-  uint8_t* k16 = q16 + 2 * C::QB;                            // NB K buffers
+  uint8_t* q16 = raw + NR * C::RAWS;                         // 2 query tiles (none for NQ 1)
+  uint8_t* k16 = q16 + C::QSM;                               // NB K buffers
   uint8_t* vt16 = k16 + NB * C::KB;                          // NB V^T buffers
   uint8_t* scb = vt16 + NB * C::VTB;                         // NB scale buffers
   float* rowf = reinterpret_cast<float*>(scb + NB * C::SCS); // [2][128] score factor per row
@@ -148,14 +166,14 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   const int q0 = pa.query_start[b];
   const int n_b = pa.query_start[b + 1] - q0;
   const int L = a.context_lens[b];
-  if (ct * 2 * QP >= n_b || n_b <= 0) return;               // whole CTA: before any barrier
+  if (ct * NQ * QP >= n_b || n_b <= 0) return;              // whole CTA: before any barrier
   if (L < n_b || (long long)L > ((long long)a.max_blocks << a.bs_shift)) {
     if (tid == 0) atomicOr(a.err, ERR_BAD_INDEX);
     return;
   }
-  const int qbase = ct * 2 * QP;                            // query index of tile 0, row 0
+  const int qbase = ct * NQ * QP;                           // query index of tile 0, row 0
   const int first = L - n_b + qbase;                        // its position
-  const int nq = min(2 * QP, n_b - qbase);                  // valid query positions here
+  const int nq = min(NQ * QP, n_b - qbase);                 // valid query positions here
   const int pmax = first + nq - 1;
   const int kmin = (a.window > 0) ? max(0, first + 1 - a.window) : 0;
   const int t0 = kmin / WKT, t1 = pmax / WKT;               // key tiles, inclusive
@@ -185,57 +203,111 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
                  "r"(C::TCOLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
 
-  // ---- queries of both tiles: row R = 128 j + h * QP + i -> query index
+  // ---- queries: row R = 128 j + h * QP + i of query tile j -> query index
   // qbase + j * QP + i, head g*G + h, prescaled by a power of two so the bf16
-  // values are exact in f16.  Lane l holds elements l + 32e of the row.
+  // values are exact in f16.
   float ks_static = 1.f;
   if constexpr (MODE == FP8_PER_TENSOR) ks_static = a.k_scale[0];
   if constexpr (MODE == FP8_PER_HEAD) ks_static = a.k_scale[g];
-  for (int R = warp; R < 2 * WROWS; R += WS_THREADS / 32) {
-    const int j = R / WROWS, r = R - j * WROWS;
-    const int h = r / QP, i = r - h * QP;
-    const int qi = j * QP + i;                               // query index within the CTA
-    const bool valid = qi < nq;
-    constexpr int EL = D / 32;
-    float x[EL];
-    float amax = 0.f;
-    if (valid) {
-      const uint16_t* src = a.q + ((long long)(q0 + qbase + qi) * a.Hq + g * G + h) * D;
+  if constexpr (NQ == 2) {
+    // into shared memory (K-major, 128-byte swizzle); lane l holds elements
+    // l + 32e of the row
+    for (int R = warp; R < NQ * WROWS; R += RL::THREADS / 32) {
+      const int j = R / WROWS, r = R - j * WROWS;
+      const int h = r / QP, i = r - h * QP;
+      const int qi = j * QP + i;                             // query index within the CTA
+      const bool valid = qi < nq;
+      constexpr int EL = D / 32;
+      float x[EL];
+      float amax = 0.f;
+      if (valid) {
+        const uint16_t* src = a.q + ((long long)(q0 + qbase + qi) * a.Hq + g * G + h) * D;
+#pragma unroll
+        for (int e = 0; e < EL; ++e) {
+          x[e] = __uint_as_float((uint32_t)src[lane + 32 * e] << 16);
+          amax = fmaxf(amax, fabsf(x[e]));
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < EL; ++e) x[e] = 0.f;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      int qexp = 0;
+      if (amax > 0.f) qexp = max(((int)(__float_as_uint(amax) >> 23) & 0xFF) - 127, -100);
+      const float qmul = pow2i(14 - qexp);
+      uint8_t* qt = q16 + j * C::QB;
 #pragma unroll
       for (int e = 0; e < EL; ++e) {
-        x[e] = __uint_as_float((uint32_t)src[lane + 32 * e] << 16);
-        amax = fmaxf(amax, fabsf(x[e]));
+        const int d = lane + 32 * e;
+        const uint16_t h16 = (uint16_t)(pack_f16x2(x[e] * qmul, 0.f) & 0xFFFFu);
+        *reinterpret_cast<uint16_t*>(qt + (d >> 6) * (WROWS * 128) + swc(r, (d & 63) >> 3) + (d & 7) * 2) = h16;
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < EL; ++e) x[e] = 0.f;
+      if (lane == 0) {
+        rowf[R] = a.qk_scale * ks_static * pow2i(qexp - 14);
+        rowp[R] = valid ? first + qi : -1;
+      }
     }
+  } else {
+    // into tensor memory, the A operand of S: the softmax warps' thread r
+    // owns row r (its lane) and stores its D / 2 f16 pairs as columns
+    if (warp < RL::SOFT) {
+      const int r = warp * 32 + lane;
+      const int h = r / QP, i = r - h * QP;
+      const bool valid = i < nq;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + ((long long)(q0 + qbase + (valid ? i : 0)) * a.Hq + g * G + h) * D);
+      float amax = 0.f;
+      if (valid) {
+#pragma unroll 4
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 v = src[c];
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    int qexp = 0;
-    if (amax > 0.f) qexp = max(((int)(__float_as_uint(amax) >> 23) & 0xFF) - 127, -100);
-    const float qmul = pow2i(14 - qexp);
-    uint8_t* qt = q16 + j * C::QB;
+          for (int e = 0; e < 4; ++e)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w4[e] << 16)),
+                                     fabsf(__uint_as_float(w4[e] & 0xFFFF0000u))));
+        }
+      }
+      int qexp = 0;
+      if (amax > 0.f) qexp = max(((int)(__float_as_uint(amax) >> 23) & 0xFF) - 127, -100);
+      const float qmul = pow2i(14 - qexp);
+      const uint32_t trq = tmem + ((uint32_t)(warp * 32) << 16) + C::QCOL;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {     // 32 columns = 64 elements at a time
+        uint32_t wq[32];
 #pragma unroll
-    for (int e = 0; e < EL; ++e) {
-      const int d = lane + 32 * e;
-      const uint16_t h16 = (uint16_t)(pack_f16x2(x[e] * qmul, 0.f) & 0xFFFFu);
-      *reinterpret_cast<uint16_t*>(qt + (d >> 6) * (WROWS * 128) + swc(r, (d & 63) >> 3) + (d & 7) * 2) = h16;
-    }
-    if (lane == 0) {
-      rowf[R] = a.qk_scale * ks_static * pow2i(qexp - 14);
-      rowp[R] = valid ? first + qi : -1;
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = valid ? src[(c0 * 2) / 8 + c] : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            wq[4 * c + e] = pack_f16x2(__uint_as_float(w4[e] << 16) * qmul,
+                                       __uint_as_float(w4[e] & 0xFFFF0000u) * qmul);
+        }
+        uint32_t lo16[16], hi16[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) { lo16[e] = wq[e]; hi16[e] = wq[16 + e]; }
+        tmem_st16_nowait(trq + c0, lo16);
+        tmem_st16_nowait(trq + c0 + 16, hi16);
+      }
+      tmem_wait_st();
+      rowf[r] = a.qk_scale * ks_static * pow2i(qexp - 14);
+      rowp[r] = valid ? first + i : -1;
     }
   }
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *s_tmem;
 
   // ================================================================ roles
-  if (warp == WS_PROD) {
+  if (warp == RL::PROD) {
     // ---- producer: key tile t into raw stage (t - t0) % NR; lane s < SUB
     // copies page tile s.  Page tiles wholly outside [kmin, pmax] are not
     // fetched.
@@ -293,9 +365,9 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
 #pragma unroll
       for (int s = 0; s < NR; ++s)
         if (last[s] >= 0) (void)mbar_wait(&raw_full[s], (uint32_t)((last[s] / NR) & 1));
-  } else if (warp >= WS_SOFT && warp < WS_PROD) {
+  } else if (warp >= RL::SOFT && warp < RL::PROD) {
     // ---- converters (128 threads)
-    const int ct_ = tid - WS_SOFT * 32;
+    const int ct_ = tid - RL::SOFT * 32;
     for (int i = 0; i < ntl; ++i) {
       const int st = i % NR, buf = i % NB;
       const int t = t0 + i;
@@ -349,13 +421,19 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
         // the warp, so the 4-byte loads and the 16-byte stores of a warp meet
         // no bank twice.
         constexpr int DG = D / 4;                   // d groups of 4
-        constexpr int NT = 8 * DG / (WS_CONV * 32); // tasks per thread (2 at D 128, 1 at D 64)
+        constexpr int NT = 8 * DG / (WS_CONV * 32); // tasks per thread (4 at D 256, 2 at 128, 1 at 64)
         static_assert(NT * WS_CONV * 32 == 8 * DG, "V^T tasks per converter thread");
-        const int cw = warp - WS_SOFT;              // converter warp 0..3
-        const int dg = lane % DG, hs = lane / DG;
+        const int cw = warp - RL::SOFT;              // converter warp 0..3
 #pragma unroll
         for (int it = 0; it < NT; ++it) {
-          const int kg = (((dg >> 1) + cw) & 3) + 4 * (it + hs);
+          int dg, kg;
+          if constexpr (DG > 32) {                  // D 256: two sweeps of 32 d groups
+            dg = lane + 32 * (it & 1);
+            kg = (((lane >> 1) + cw) & 3) + 4 * (it >> 1);
+          } else {
+            dg = lane % DG;
+            kg = (((dg >> 1) + cw) & 3) + 4 * (it + lane / DG);
+          }
           uint32_t x[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -394,9 +472,15 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
         // then gives the f16 values of d = 2bb (low nibbles) and 2bb + 1 (high
         // nibbles, read 16x and scaled back exactly).
         constexpr int BG = D / 8;                   // 4-byte groups of a key row
-        const int cw = warp - WS_SOFT;
+        constexpr int NTI = (8 * BG > WS_CONV * 32) ? 8 * BG / (WS_CONV * 32) : 1;
+        const int cw = warp - RL::SOFT;
+#pragma unroll
+        for (int it = 0; it < NTI; ++it) {
         int bg, kg;
-        if constexpr (BG >= 16) {                   // 128 tasks, one per thread
+        if constexpr (BG >= 32) {                   // D 256: 256 tasks, two per thread
+          bg = lane;
+          kg = (((lane >> 1) + cw) & 3) + 4 * it;
+        } else if constexpr (BG >= 16) {            // 128 tasks, one per thread
           bg = lane % BG;
           kg = (((bg >> 1) + cw) & 3) + 4 * (lane / BG);
         } else {                                    // 64 tasks: the first 64 threads
@@ -444,6 +528,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
             *reinterpret_cast<uint4*>(vb + swc(d + 1, kg)) = make_uint4(od[0], od[1], od[2], od[3]);
           }
         }
+        }
       }
       {
         // scales: threads 0..63 K, 64..127 V (scale 0: no key)
@@ -474,7 +559,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
         mbar_arrive(&kv_full[buf]);
       }
     }
-  } else if (warp == WS_MMA) {
+  } else if (warp == RL::MMA) {
     // ---- MMA issuer: one elected lane issues and commits (elect.sync picks
     // the same lane each time: the warp is converged); the warp waits together
     constexpr uint32_t IDS = mma_idesc<false>(WROWS, WKT);
@@ -488,17 +573,23 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     // o is the start's descriptor plus o / 16 (the 14-bit address field
     // cannot carry: shared memory ends below 2^18 bytes)
     const uint64_t dq = sw128_desc(q16), dk = sw128_desc(k16), dv = sw128_desc(vt16);
-    // S_j = Q_j K^T from K buffer kbuf into S buffer sb of query tile j
+    // S_j = Q_j K^T from K buffer kbuf into S buffer sb of query tile j (Q
+    // from shared memory with two query tiles, from tensor memory with one)
     auto issue_s = [&](int j, int kbuf, int sb) {
       const uint64_t qa = dq + (uint64_t)(j * (C::QB >> 4));
       const uint64_t kb = dk + (uint64_t)(kbuf * (C::KB >> 4));
-      const uint32_t td = tmem + 64 * (2 * j + sb);
+      const uint32_t td = tmem + C::scol(j, sb);
       if (elect_one()) {
         tc_fence_after();
 #pragma unroll
-        for (int s2 = 0; s2 < D / 16; ++s2)
-          umma(td, qa + (uint64_t)((((s2 >> 2) * (WROWS * 128)) + (s2 & 3) * 32) >> 4),
-               kb + (uint64_t)((((s2 >> 2) * (WKT * 128)) + (s2 & 3) * 32) >> 4), IDS, s2 > 0);
+        for (int s2 = 0; s2 < D / 16; ++s2) {
+          const uint64_t db = kb + (uint64_t)((((s2 >> 2) * (WKT * 128)) + (s2 & 3) * 32) >> 4);
+          if constexpr (NQ == 2)
+            umma(td, qa + (uint64_t)((((s2 >> 2) * (WROWS * 128)) + (s2 & 3) * 32) >> 4), db, IDS,
+                 s2 > 0);
+          else
+            umma_tmem_a(td, tmem + C::QCOL + 8 * s2, db, IDS, s2 > 0);
+        }
         umma_commit(&s_full[2 * j + sb]);
       }
       __syncwarp();
@@ -507,8 +598,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     // from buffer vbuf
     auto issue_pv = [&](int j, int vbuf, int sb, bool acc) {
       const uint64_t vb = dv + (uint64_t)(vbuf * (C::VTB >> 4));
-      const uint32_t td = tmem + C::OCOL + D * j;
-      const uint32_t ta = tmem + 64 * (2 * j + sb);
+      const uint32_t td = tmem + C::ocol(j);
+      const uint32_t ta = tmem + C::scol(j, sb);
       if (elect_one()) {
         tc_fence_after();
 #pragma unroll
@@ -524,37 +615,37 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     // PV_j(t), the last reader of that buffer's P', has completed, so the
     // softmax of a query tile finds its next scores ready when it finishes
     if (wait(&kv_full[0], 0u)) {
-      issue_s(0, 0, 0);
-      issue_s(1, 0, 0);
+#pragma unroll
+      for (int j = 0; j < NQ; ++j) issue_s(j, 0, 0);
       bool go = true;
       if (ntl > 1) {
         go = wait(&kv_full[1 % NB], (uint32_t)((1 / NB) & 1));
-        if (go) {
-          issue_s(0, 1 % NB, 1);
-          issue_s(1, 1 % NB, 1);
-        }
+        if (go)
+#pragma unroll
+          for (int j = 0; j < NQ; ++j) issue_s(j, 1 % NB, 1);
       }
       for (int i = 0; go && i < ntl; ++i) {
         const int buf = i % NB, sb = i & 1;
-        if (!wait(&p_full[sb], (uint32_t)((i >> 1) & 1))) break;
-        issue_pv(0, buf, sb, i > 0);
-        if (elect_one()) umma_commit(&pv_done[0]);
-        __syncwarp();
-        if (!wait(&p_full[2 + sb], (uint32_t)((i >> 1) & 1))) break;
-        issue_pv(1, buf, sb, i > 0);
-        // both PVs of this key tile have read its operands: buffer free
-        if (elect_one()) {
-          umma_commit(&pv_done[1]);
-          umma_commit(&kv_empty[buf]);
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          if (!wait(&p_full[2 * j + sb], (uint32_t)((i >> 1) & 1))) { go = false; break; }
+          issue_pv(j, buf, sb, i > 0);
+          if (elect_one()) umma_commit(&pv_done[j]);
+          __syncwarp();
         }
+        if (!go) break;
+        // every PV of this key tile has read its operands: buffer free
+        if (elect_one()) umma_commit(&kv_empty[buf]);
         __syncwarp();
         if (i + 2 < ntl) {
           const int nb2 = (i + 2) % NB;
           if (!wait(&kv_full[nb2], (uint32_t)(((i + 2) / NB) & 1))) break;
-          if (!wait(&pv_done[0], (uint32_t)(i & 1))) break;
-          issue_s(0, nb2, sb);
-          if (!wait(&pv_done[1], (uint32_t)(i & 1))) break;
-          issue_s(1, nb2, sb);
+#pragma unroll
+          for (int j = 0; j < NQ; ++j) {
+            if (!wait(&pv_done[j], (uint32_t)(i & 1))) { go = false; break; }
+            issue_s(j, nb2, sb);
+          }
+          if (!go) break;
         }
       }
     }
@@ -571,7 +662,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     const int loA = (a.window > 0) ? max(0, pA + 1 - a.window) : 0;
     const float fA = rowf[R];
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t tO = trow + C::OCOL + D * j;
+    const uint32_t tO = trow + C::ocol(j);
     // positions of this query tile's first and last rows: a key tile inside
     // [last row's window start, first row] is visible to every row
     const int firstj = first + j * QP;
@@ -589,7 +680,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       const int buf = i % NB, t = t0 + i;
       // S of this tile in S/P' buffer i & 1 (its P' replaces it there)
       const int sb = i & 1;
-      const uint32_t tS = trow + 64 * (2 * j + sb), tP = tS;
+      const uint32_t tS = trow + C::scol(j, sb), tP = tS;
       const bool w = __all_sync(0xffffffffu, mbar_wait(&s_full[2 * j + sb], (uint32_t)((i >> 1) & 1)));
       if (!w && lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
       if (!w || __any_sync(0xffffffffu, *s_abort)) { ok = false; break; }
@@ -763,11 +854,11 @@ cudaError_t wslaunch3(const PrefillArgs& pa0, int max_query_len, cudaStream_t st
     attr_set[dev] = true;
   }
   PrefillArgs pa = pa0;
-  const int qp2 = 2 * (WROWS / G);                  // query positions per CTA
+  const int qp2 = WRoles<D>::NQ * (WROWS / G);      // query positions per CTA
   pa.qtiles = (max_query_len + qp2 - 1) / qp2;
   const long long grid = (long long)pa.qtiles * a.B * a.Hkv;
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, WS_THREADS, C::SMEM, st>>>(pa, km, vm);
+  kern<<<(unsigned)grid, WRoles<D>::THREADS, C::SMEM, st>>>(pa, km, vm);
   return cudaGetLastError();
 }
 
@@ -787,13 +878,14 @@ cudaError_t wslaunch1(int D, int G, const PrefillArgs& pa, int mq, cudaStream_t 
   switch (D) {
     case 64: return wslaunch2<MODE, 64>(G, pa, mq, st);
     case 128: return wslaunch2<MODE, 128>(G, pa, mq, st);
+    case 256: return wslaunch2<MODE, 256>(G, pa, mq, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-bool prefill_ws_supports(int mode, int D) { return mode != BF16 && (D == 64 || D == 128); }
+bool prefill_ws_supports(int mode, int D) { return mode != BF16 && (D == 64 || D == 128 || D == 256); }
 
 cudaError_t launch_prefill_ws(int mode, int D, int G, const DecodeArgs& a, const int* query_start,
                               int max_query_len, cudaStream_t st) {
