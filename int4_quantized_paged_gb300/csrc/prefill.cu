@@ -1,9 +1,9 @@
 // Prefill (chunked multi-query) attention over the quantized paged cache on
 // the fifth-generation tensor cores (tcgen05, accumulators in tensor memory),
-// single-role: every warp takes each phase in turn.  It serves BF16 layers and
-// head_dim 256, whose operands do not fit the warp-specialised kernel's two
-// query tiles; FP8 and INT4 layers of head_dim 64 and 128 go to that kernel
-// (launch_prefill below dispatches).
+// single-role: every warp takes each phase in turn.  It serves BF16 layers,
+// whose three-term split of P' does not fit the warp-specialised kernel's
+// tensor-memory layout; FP8 and INT4 layers go to that kernel (launch_prefill
+// below dispatches).
 //
 // What it computes: sequence b appends n_b tokens at positions
 // [L_b - n_b, L_b) (their K/V already written by the cache write); each new

@@ -1,5 +1,5 @@
 // Prefill (chunked multi-query) attention over a quantized paged cache (FP8 or
-// INT4 codes, head_dim 64 or 128), warp-specialised on the fifth-generation
+// INT4 codes, head_dim 64, 128 or 256), warp-specialised on the fifth-generation
 // tensor cores.  It computes what the single-role prefill kernel computes
 // (causal attention of each new token's query over the retained positions,
 // the scales folded into score and weight: "Per-tensor vs per-head FP8 KV
@@ -10,7 +10,10 @@
 //
 // A CTA owns two query tiles of M = 128 rows each (128/G consecutive new
 // positions times the G query heads of one KV head; tile 1 follows tile 0),
-// and streams the keys of both in tiles of 64 positions.  Roles (14 warps):
+// and streams the keys of both in tiles of 64 positions.  At head_dim 256 a
+// CTA owns one query tile (its O takes 256 tensor-memory columns) and keeps
+// Q in tensor memory, the A operand of S; the roles below then have one
+// softmax warpgroup and the other warps move down by four.  Roles (14 warps):
 //  * warp 12, producer: 2-D TMA copies of the key tile's K and V page tiles
 //    (and 64-byte bulk copies of their dynamic scales) into a ring of raw
 //    stages; lane s takes page tile s.
