@@ -284,7 +284,9 @@ kvq_status kvq_decode_attention_bf16(const kvq_ctx* ctx, int layer, const void* 
  * Scale pointers and block table as for kvq_decode_attention.  No workspace;
  * n_b > L_b, or L_b beyond the positions the sequence's block-table row
  * covers (max_blocks_per_seq x block_size), sets the BAD_INDEX bit of the
- * device error word and skips that sequence. */
+ * device error word and skips that sequence; a block id outside
+ * [0, num_blocks) sets the same bit, nothing is read for that page, and its
+ * positions are left out of the softmax (the output stays finite). */
 kvq_status kvq_prefill_attention(const kvq_ctx* ctx, int layer, const void* q,
                                  const void* k_cache, const void* v_cache, const float* k_scale,
                                  const float* v_scale, const float* k_cache_scale,
