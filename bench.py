@@ -18,7 +18,7 @@ measured HBM peak, per-kernel CUDA-event times) and a few prefill chunks (the
                     [--no-prefill]
                     [--batch B] [--context L] [--layer I]     # smaller cases (profiling)
     python bench.py --impl reference     # the CPU oracle on a bounded sample
-    python bench.py --prefill --workload llama8b|gemma_d256     # prefill TFLOP/s
+    python bench.py --prefill --workload llama8b|gemma_d256|gptoss20b     # prefill TFLOP/s
     python bench.py --latency-sweep --workload gptoss20b        # latency vs context
 
 Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
@@ -688,6 +688,7 @@ PREFILL_BLOCK = [
     ("llama8b", "fp8_per_head"),
     ("llama8b", "int4_per_token_head"),
     ("gemma_d256", "fp8_per_token_head"),
+    ("gptoss20b", "fp8_per_token_head"),
 ]
 
 
@@ -940,6 +941,8 @@ PREFILL = {
                 "Hq=32 Hkv=8 D=128", 4, 3072, 1024),
     "gemma_d256": ("Gemma-like prefill chunk: 8192 new tokens at positions [8192, 16384) of one "
                    "sequence, Hq=16 Hkv=8 D=256, full-attention layer", 1, 8192, 8192),
+    "gptoss20b": ("gpt-oss-like prefill chunk: 4 sequences x 1024 new tokens after 3072 cached, "
+                  "Hq=64 Hkv=8 D=64, full-attention layer", 4, 3072, 1024),
 }
 
 
