@@ -1,7 +1,8 @@
 """Prefill at the group sizes the workloads do not use, on both prefill
 kernels' shapes: G = 1 (a query tile of 128 positions, so the two query tiles
 of one CTA span 256 positions, wider than a 100-token window) and G = 2, at
-head_dim 64 and 128, window and full layers, quantized modes (the
+head_dim 64, 128 and 256 (one query tile per CTA, Q in tensor memory), window
+and full layers, quantized modes (the
 warp-specialised kernel) and BF16 (the single-role kernel), with ragged
 chunks that leave the second query tile of the last CTA partly or wholly
 empty.  Each output row is checked against the oracle's prefill with the
@@ -20,6 +21,7 @@ SHAPES = {
     "g1-d128": (8, 8, 128, (700, 333, 300), (300, 77, 256)),
     "g2-d64": (8, 4, 64, (650, 129), (257, 129)),
     "g1-d64": (4, 4, 64, (520, 40), (400, 40)),
+    "g1-d256": (4, 4, 256, (530, 300), (260, 300)),
 }
 
 
