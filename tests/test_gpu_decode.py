@@ -50,9 +50,13 @@ def test_tiny_per_tensor_one_control():
 
 @pytest.mark.parametrize("mode", [orc.FP8_PER_TOKEN_HEAD, orc.INT4_PER_TOKEN_HEAD, orc.BF16])
 @pytest.mark.parametrize("window", [0, 40])
-def test_ragged_and_empty_contexts(mode, window):
-    base = SMALL["llama8b"]
-    w = wl.Workload("ragged", Hq=32, Hkv=8, D=128, block_size=16,
+@pytest.mark.parametrize("D", [128, 64])
+def test_ragged_and_empty_contexts(mode, window, D):
+    """Contexts that end inside a 16-position page tile, on its boundary and
+    one past it, with and without a window (window starts inside a tile), at
+    head_dim 128 and 64 (1 KB page tiles for FP8, 512 bytes for INT4), each
+    with one, several and the automatic number of workers."""
+    w = wl.Workload("ragged", Hq=32, Hkv=8, D=D, block_size=16,
                     context_lens=(0, 1, 15, 16, 17, 33, 250, 1000), windows=(window,),
                     head_mult_loguniform=(0.5, 32.0), outlier_p=0.01, outlier_factor=8.0,
                     seed=77)
@@ -61,7 +65,7 @@ def test_ragged_and_empty_contexts(mode, window):
     for workers in (1, 4, 13, 0):
         out = r.decode(num_workers=workers)
         assert torch.all(out[0] == 0), "empty context must give zeros"
-        r.check_decode(out, where=f"ragged w{window} workers {workers}")
+        r.check_decode(out, where=f"ragged D{D} w{window} workers {workers}")
 
 
 def test_shorter_context_than_written_and_worker_independence():
