@@ -58,6 +58,19 @@ namespace {
 constexpr int WS_CONV = 4;                          // converter warps
 constexpr int WROWS = 128;                          // rows per query tile (the MMA's M)
 
+// A 16-byte shared-memory load that stays after the tensor-memory stores
+// issued before it (both are volatile asm): the softmax reads a chunk's V
+// scales just before it uses them, instead of the compiler hoisting all
+// sixteen loads of a tile to its start, where their 64 registers pushed the
+// thread past its 128-register share and spilled.
+__device__ __forceinline__ float4 lds_v4_ordered(const float4* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"((uint32_t)__cvta_generic_to_shared(p)));
+  return v;
+}
+
 // Warp roles: NQ query tiles per CTA (two at head_dim 64 and 128; one at 256,
 // whose O needs 256 tensor-memory columns), a softmax warpgroup per query
 // tile, then the converters, the producer and the MMA issuer.
@@ -787,7 +800,7 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
             lp[e] += x[e];
           }
           if constexpr (C::DYN) {
-            const float4 vq = vs4[k >> 2];
+            const float4 vq = lds_v4_ordered(vs4 + (k >> 2));
             x[0] *= vq.x; x[1] *= vq.y; x[2] *= vq.z; x[3] *= vq.w;
           }
 #pragma unroll
