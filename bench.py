@@ -1027,7 +1027,7 @@ def run_prefill(args):
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                          "kernel": ("prefill_ws_kernel (tcgen05, warp-specialised, P' f16 hi + lo "
-                                    "in tensor memory)" if mode != kvq.BF16 and w.D in (64, 128, 256)
+                                    "in tensor memory)" if w.D in ((64, 128) if mode == kvq.BF16 else (64, 128, 256))
                                     else "prefill_tc_kernel (tcgen05, P' split in shared memory)"),
                          "peak_source": f"{src} bf16 dense"},
             "gpu_launches": n, "clocks": clocks}

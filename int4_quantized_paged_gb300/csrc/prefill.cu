@@ -1,9 +1,9 @@
 // Prefill (chunked multi-query) attention over the quantized paged cache on
 // the fifth-generation tensor cores (tcgen05, accumulators in tensor memory),
-// single-role: every warp takes each phase in turn.  It serves BF16 layers,
-// whose three-term split of P' does not fit the warp-specialised kernel's
-// tensor-memory layout; FP8 and INT4 layers go to that kernel (launch_prefill
-// below dispatches).
+// single-role: every warp takes each phase in turn.  It serves BF16 layers
+// at head_dim 256, whose bf16 pages do not fit the warp-specialised kernel's
+// raw stages beside its operand buffers; every other layer goes to that
+// kernel (launch_prefill below dispatches).
 //
 // What it computes: sequence b appends n_b tokens at positions
 // [L_b - n_b, L_b) (their K/V already written by the cache write); each new

@@ -93,10 +93,17 @@ struct WCfg {
   static constexpr int RB = row_bytes<MODE>(D);
   static constexpr int TB = 16 * RB;                       // one page tile (16 positions)
   static constexpr int TBP = (TB + 1023) / 1024 * 1024;
-  static constexpr bool DYN = (MODE == FP8_PER_TOKEN_HEAD || MODE == INT4_PER_TOKEN_HEAD);
+  // scales copied from the cache with the codes (dynamic FP8, INT4)
+  static constexpr bool FETCH = (MODE == FP8_PER_TOKEN_HEAD || MODE == INT4_PER_TOKEN_HEAD);
+  // BF16 layers: K stays bf16 (S is a bf16 MMA against bf16 queries); each V
+  // row is scaled by the power of two that maps its largest exponent to 2^14
+  // and converted to f16 exactly, and its V scale is that power's inverse
+  static constexpr bool BFK = (MODE == BF16);
+  // per-key V scales in the scale buffer, followed by the softmax's range factor
+  static constexpr bool DYN = FETCH || BFK;
   static constexpr int SUB = WKT / 16;                      // page tiles per key tile
   static constexpr int RAW = 2 * SUB * TBP;                 // K and V page tiles of a key tile
-  static constexpr int SCB = DYN ? 2 * SUB * 64 : 0;        // their K and V scales
+  static constexpr int SCB = FETCH ? 2 * SUB * 64 : 0;      // their K and V scales
   static constexpr int RAWS = (RAW + SCB + 1023) / 1024 * 1024;
   static constexpr int NQ = WRoles<D>::NQ;
   static constexpr int QB = WROWS * D * 2;                  // one query tile: D/64 blocks of 128 x 128 B
@@ -143,7 +150,7 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
   constexpr int NB = C::NB;
   constexpr int QP = WROWS / G;                // positions per query tile
   constexpr int CPR = C::RB / 16;              // 16-byte raw chunks per position row
-  constexpr int EPC = (MODE == INT4_PER_TOKEN_HEAD) ? 32 : 16;   // elements per raw chunk
+  constexpr int EPC = (MODE == INT4_PER_TOKEN_HEAD) ? 32 : (MODE == BF16 ? 8 : 16);   // elements per raw chunk
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -226,7 +233,7 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
 
   // ---- queries: row R = 128 j + h * QP + i of query tile j -> query index
   // qbase + j * QP + i, head g*G + h, prescaled by a power of two so the bf16
-  // values are exact in f16.
+  // values are exact in f16 (BF16 layers: the bf16 values as they are).
   float ks_static = 1.f;
   if constexpr (MODE == FP8_PER_TENSOR) ks_static = a.k_scale[0];
   if constexpr (MODE == FP8_PER_HEAD) ks_static = a.k_scale[g];
@@ -256,12 +263,14 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       int qexp = 0;
       if (amax > 0.f) qexp = max(((int)(__float_as_uint(amax) >> 23) & 0xFF) - 127, -100);
+      if constexpr (C::BFK) qexp = 14;
       const float qmul = pow2i(14 - qexp);
       uint8_t* qt = q16 + j * C::QB;
 #pragma unroll
       for (int e = 0; e < EL; ++e) {
         const int d = lane + 32 * e;
-        const uint16_t h16 = (uint16_t)(pack_f16x2(x[e] * qmul, 0.f) & 0xFFFFu);
+        const uint16_t h16 = C::BFK ? (uint16_t)(__float_as_uint(x[e]) >> 16)
+                                    : (uint16_t)(pack_f16x2(x[e] * qmul, 0.f) & 0xFFFFu);
         *reinterpret_cast<uint16_t*>(qt + (d >> 6) * (WROWS * 128) + swc(r, (d & 63) >> 3) + (d & 7) * 2) = h16;
       }
       if (lane == 0) {
@@ -359,7 +368,7 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
       fence_proxy_async();
       if (lane == 0) {
         s_have[st] = (int)fetch;
-        mbar_expect_tx(&raw_full[st], (uint32_t)__popc(fetch) * (2 * C::TB + (C::DYN ? 128 : 0)));
+        mbar_expect_tx(&raw_full[st], (uint32_t)__popc(fetch) * (2 * C::TB + (C::FETCH ? 128 : 0)));
       }
       __syncwarp();
       if (want) {
@@ -368,7 +377,7 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
         const int rowc = (int)(((unsigned long long)cell * C::RB) >> 7);
         tma_tile_2d(base + lane * C::TBP, &kmap, 0, rowc, &raw_full[st]);
         tma_tile_2d(base + (SUB + lane) * C::TBP, &vmap, 0, rowc, &raw_full[st]);
-        if constexpr (C::DYN) {
+        if constexpr (C::FETCH) {
           float* sc = reinterpret_cast<float*>(base + C::RAW);
           bulk_copy(sc + 16 * lane, a.k_cs + cell, 64, &raw_full[st]);
           bulk_copy(sc + 16 * (SUB + lane), a.v_cs + cell, 64, &raw_full[st]);
@@ -428,7 +437,83 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
         }
       }
       uint8_t* vb = vt16 + buf * C::VTB;
-      if constexpr (MODE != INT4_PER_TOKEN_HEAD) {
+      if constexpr (MODE == BF16) {
+        // V of a BF16 layer.  First the largest exponent e of each key row
+        // (two threads per key, half a row each): the key's V scale is
+        // 2^(e - 14), and the row times 2^(14 - e) has its largest value in
+        // [2^14, 2^15), so every bf16 value down to 2^-28 of it converts to
+        // f16 exactly.
+        float* vsm = reinterpret_cast<float*>(scb + buf * C::SCS) + WKT;
+        {
+          const int key = ct_ >> 1, hh = ct_ & 1;
+          const int sub = key >> 4, kr = key & 15;
+          const int pos = t * WKT + key;
+          const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
+          uint32_t em = 0;                          // exponent fields (<< 7) of both halves of a word
+          if (live) {
+#pragma unroll
+            for (int c = 0; c < CPR / 2; ++c) {
+              const uint4 w = *reinterpret_cast<const uint4*>(
+                  base + (SUB + sub) * C::TBP + swz((uint32_t)(kr * C::RB + (hh * (CPR / 2) + c) * 16)));
+              em = __vmaxu2(em, w.x & 0x7F807F80u);
+              em = __vmaxu2(em, w.y & 0x7F807F80u);
+              em = __vmaxu2(em, w.z & 0x7F807F80u);
+              em = __vmaxu2(em, w.w & 0x7F807F80u);
+            }
+          }
+          em = max(em & 0xFFFFu, em >> 16) >> 7;    // biased exponent, 0 for zeros
+          em = max(em, __shfl_xor_sync(0xffffffffu, em, 1));
+          const int e = em ? max((int)em - 127, -100) : 0;
+          if (hh == 0) vsm[key] = live ? pow2i(e - 14) : 0.f;
+        }
+        named_sync(CONV_BAR, WS_CONV * 32);         // every key's V scale is in place
+        // V^T: a task is 8 keys x one d pair (one word per key).  Each key's
+        // two values are scaled by the inverse of its V scale (a power of two:
+        // exact) and packed, keys 2q and 2q + 1 per word, into the rows of
+        // d = 2 dp (low halves) and 2 dp + 1 (high halves).  Consecutive
+        // lanes take consecutive d pairs of the same keys (one 128-byte row
+        // per load), and lanes with bit 2 set store their odd row first, so
+        // that each 8-lane phase of a store meets every bank once.
+        constexpr int DP = D / 2;
+        constexpr int NTB = 8 * DP / (WS_CONV * 32);
+        static_assert(NTB * WS_CONV * 32 == 8 * DP, "V^T tasks per converter thread");
+#pragma unroll
+        for (int it = 0; it < NTB; ++it) {
+          const int task = ct_ + it * WS_CONV * 32;
+          const int dp = task % DP, kg = task / DP;
+          const float4 s0 = *reinterpret_cast<const float4*>(vsm + 8 * kg);
+          const float4 s1 = *reinterpret_cast<const float4*>(vsm + 8 * kg + 4);
+          const float sk[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+          uint32_t x[8];
+          float inv[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int key = 8 * kg + k;
+            const int sub = key >> 4, kr = key & 15;
+            const int pos = t * WKT + key;
+            const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
+            x[k] = live ? *reinterpret_cast<const uint32_t*>(base + (SUB + sub) * C::TBP +
+                                                            swz((uint32_t)(kr * C::RB + 4 * dp)))
+                        : 0u;
+            // 2^(14 - e) from 2^(e - 14); 2^127 for a key with no data (its values are 0)
+            inv[k] = __uint_as_float((254u - (__float_as_uint(sk[k]) >> 23)) << 23);
+          }
+          uint32_t ev[4], od[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            ev[q] = pack_f16x2(__uint_as_float(x[2 * q] << 16) * inv[2 * q],
+                               __uint_as_float(x[2 * q + 1] << 16) * inv[2 * q + 1]);
+            od[q] = pack_f16x2(__uint_as_float(x[2 * q] & 0xFFFF0000u) * inv[2 * q],
+                               __uint_as_float(x[2 * q + 1] & 0xFFFF0000u) * inv[2 * q + 1]);
+          }
+          const uint4 E = make_uint4(ev[0], ev[1], ev[2], ev[3]);
+          const uint4 O = make_uint4(od[0], od[1], od[2], od[3]);
+          const bool swp = (lane >> 2) & 1;
+          *reinterpret_cast<uint4*>(vb + swc(2 * dp + (swp ? 1 : 0), kg)) = swp ? O : E;
+          *reinterpret_cast<uint4*>(vb + swc(2 * dp + (swp ? 0 : 1), kg)) = swp ? E : O;
+        }
+      }
+      if constexpr (MODE != INT4_PER_TOKEN_HEAD && MODE != BF16) {
         // V^T straight from the raw FP8 codes: a task is 8 keys x 4 d.  Its
         // 8 words (one per key: codes of d..d+3) are transposed in registers
         // into 4 rows of 8 codes each, converted, and stored as one 16-byte
@@ -557,9 +642,14 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
         const int pos = t * WKT + key;
         const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
         float sc = live ? 1.f : 0.f;
-        if constexpr (C::DYN)
+        if constexpr (C::FETCH)
           if (live) sc = reinterpret_cast<const float*>(base + C::RAW)[16 * (isv ? SUB + sub : sub) + (key & 15)];
-        (isv ? vsm : ksm)[key] = sc;
+        if constexpr (C::BFK) {
+          if (isv) sc = vsm[key];                   // the BF16 V scale found above
+          else ksm[key] = sc;
+        } else {
+          (isv ? vsm : ksm)[key] = sc;
+        }
         if constexpr (C::DYN) {
           if (isv) {
             const int e = __reduce_max_sync(0xffffffffu, live ? f32_exp(sc) : -1000);
@@ -578,7 +668,7 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
   } else if (warp == RL::MMA) {
     // ---- MMA issuer: one elected lane issues and commits (elect.sync picks
     // the same lane each time: the warp is converged); the warp waits together
-    constexpr uint32_t IDS = mma_idesc<false>(WROWS, WKT);
+    constexpr uint32_t IDS = mma_idesc<C::BFK>(WROWS, WKT);   // bf16 Q and K for BF16 layers
     constexpr uint32_t IDO = mma_idesc<false>(WROWS, D);
     auto wait = [&](uint64_t* bar, uint32_t par) -> bool {
       const bool w = __all_sync(0xffffffffu, mbar_wait(bar, par));
@@ -899,9 +989,22 @@ cudaError_t wslaunch1(int D, int G, const PrefillArgs& pa, int mq, cudaStream_t 
   }
 }
 
+// BF16 layers at head_dim 64 and 128 (a BF16 raw stage at 256 does not fit
+// beside the operand buffers)
+cudaError_t wslaunch1_bf16(int D, int G, const PrefillArgs& pa, int mq, cudaStream_t st) {
+  switch (D) {
+    case 64: return wslaunch2<BF16, 64>(G, pa, mq, st);
+    case 128: return wslaunch2<BF16, 128>(G, pa, mq, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
 
-bool prefill_ws_supports(int mode, int D) { return mode != BF16 && (D == 64 || D == 128 || D == 256); }
+bool prefill_ws_supports(int mode, int D) {
+  if (mode == BF16) return D == 64 || D == 128;
+  return D == 64 || D == 128 || D == 256;
+}
 
 cudaError_t launch_prefill_ws(int mode, int D, int G, const DecodeArgs& a, const int* query_start,
                               int max_query_len, cudaStream_t st) {
@@ -915,6 +1018,7 @@ cudaError_t launch_prefill_ws(int mode, int D, int G, const DecodeArgs& a, const
     case FP8_PER_HEAD: return wslaunch1<FP8_PER_HEAD>(D, G, pa, max_query_len, st);
     case FP8_PER_TOKEN_HEAD: return wslaunch1<FP8_PER_TOKEN_HEAD>(D, G, pa, max_query_len, st);
     case INT4_PER_TOKEN_HEAD: return wslaunch1<INT4_PER_TOKEN_HEAD>(D, G, pa, max_query_len, st);
+    case BF16: return wslaunch1_bf16(D, G, pa, max_query_len, st);
     default: return cudaErrorInvalidValue;
   }
 }
