@@ -1,6 +1,6 @@
 // Prefill (chunked multi-query) attention over a quantized paged cache (FP8 or
-// INT4 codes, head_dim 64, 128 or 256), warp-specialised on the fifth-generation
-// tensor cores.  It computes what the single-role prefill kernel computes
+// INT4 codes at head_dim 64, 128 or 256; BF16 layers at 64 and 128),
+// warp-specialised on the fifth-generation tensor cores.  It computes what the single-role prefill kernel computes
 // (causal attention of each new token's query over the retained positions,
 // the scales folded into score and weight: "Per-tensor vs per-head FP8 KV
 // cache scales", section "Use a three-stage decision"; "FP8 KV cache layer
@@ -21,7 +21,11 @@
 //    K as 64 rows of D (K-major, 128-byte swizzle) and V transposed (D rows
 //    of 64 keys, by a byte transpose in registers); K and V scales (zero for a
 //    key outside the CTA's range or on a page that was not fetched) and the
-//    tile's largest V-scale exponent.  Three operand buffers.
+//    tile's largest V-scale exponent.  Three operand buffers.  BF16 layers:
+//    K stays bf16 (S is a bf16 MMA; at head_dim 128 the producer copies it
+//    straight into its operand buffer), and the converters give each V row
+//    the power-of-two V scale that maps its largest exponent to 2^14,
+//    converting it to f16 exactly; the rest then runs as for dynamic scales.
 //  * warp 13, MMA issuer (one thread): S_j = Q_j K^T (M 128, N 64) into
 //    tensor memory for each query tile j, and O_j += P'_j V with P'_j read
 //    from tensor memory, every term of its f16 hi + lo split.  Each query
@@ -102,8 +106,16 @@ struct WCfg {
   // per-key V scales in the scale buffer, followed by the softmax's range factor
   static constexpr bool DYN = FETCH || BFK;
   static constexpr int SUB = WKT / 16;                      // page tiles per key tile
-  static constexpr int RAW = 2 * SUB * TBP;                 // K and V page tiles of a key tile
-  static constexpr int SCB = FETCH ? 2 * SUB * 64 : 0;      // their K and V scales
+  // BF16 at head_dim 128: K is copied straight into its operand buffer, which
+  // halves the raw stage so that three raw stages and three operand buffers
+  // fit (two and two otherwise).  At 64 both already fit three and four, and
+  // the producer keeps its four-stage lookahead by staging K like V.
+  static constexpr bool KDIRECT = BFK && D == 128;
+  // a raw stage: the K and V page tiles of a key tile (V only with KDIRECT),
+  // then their scales
+  static constexpr int RAW = (KDIRECT ? 1 : 2) * SUB * TBP;
+  static constexpr int VOFF = KDIRECT ? 0 : SUB * TBP;      // V page tiles in a raw stage
+  static constexpr int SCB = FETCH ? 2 * SUB * 64 : 0;
   static constexpr int RAWS = (RAW + SCB + 1023) / 1024 * 1024;
   static constexpr int NQ = WRoles<D>::NQ;
   static constexpr int QB = WROWS * D * 2;                  // one query tile: D/64 blocks of 128 x 128 B
@@ -348,6 +360,17 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
           break;
         }
       }
+      if constexpr (C::KDIRECT) {
+        // K lands in operand buffer i % NB: wait until the MMAs of its last
+        // tile are done with it
+        if (i >= NB) {
+          const bool ok = mbar_wait(&kv_empty[i % NB], (uint32_t)((i / NB - 1) & 1));
+          if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) { *s_abort = 1; atomicOr(a.err, ERR_TIMEOUT); }
+            break;
+          }
+        }
+      }
       if (__any_sync(0xffffffffu, *s_abort)) break;
       const int t = t0 + i;
       const int pos = t * WKT + 16 * lane;
@@ -375,8 +398,17 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
         const unsigned cell = ((unsigned)blk * (unsigned)a.Hkv + (unsigned)g) * (unsigned)a.bs +
                               (unsigned)(pos & (a.bs - 1));
         const int rowc = (int)(((unsigned long long)cell * C::RB) >> 7);
-        tma_tile_2d(base + lane * C::TBP, &kmap, 0, rowc, &raw_full[st]);
-        tma_tile_2d(base + (SUB + lane) * C::TBP, &vmap, 0, rowc, &raw_full[st]);
+        if constexpr (C::KDIRECT) {
+          // bf16 K needs no conversion: each 64-d block of the page tile's 16
+          // rows goes to its rows of the K operand (K-major, 128-byte swizzle)
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h)
+            tma_tile_3d(k16 + (i % NB) * C::KB + h * (WKT * 128) + lane * (16 * 128), &kmap, 0, h,
+                        (int)cell, &raw_full[st]);
+        } else {
+          tma_tile_2d(base + lane * C::TBP, &kmap, 0, rowc, &raw_full[st]);
+        }
+        tma_tile_2d(base + C::VOFF + lane * C::TBP, &vmap, 0, rowc, &raw_full[st]);
         if constexpr (C::FETCH) {
           float* sc = reinterpret_cast<float*>(base + C::RAW);
           bulk_copy(sc + 16 * lane, a.k_cs + cell, 64, &raw_full[st]);
@@ -406,10 +438,12 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
       uint8_t* kb = k16 + buf * C::KB;
       // K into kb; zeros where nothing was fetched or the position lies
       // outside [kmin, pmax].  Each thread takes NIT chunks; all loads first,
-      // then conversions.
+      // then conversions.  (KDIRECT: the producer copied K there; rows of
+      // keys not fetched or outside [kmin, pmax] hold whatever was there, and
+      // the softmax masks their scores by their K scale 0.)
       constexpr int NIT = WKT * CPR / (WS_CONV * 32);
       static_assert(NIT * WS_CONV * 32 == WKT * CPR, "chunks per converter thread");
-      {
+      if constexpr (!C::KDIRECT) {
         uint4 wk[NIT];
 #pragma unroll
         for (int it = 0; it < NIT; ++it) {
@@ -454,7 +488,7 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < CPR / 2; ++c) {
               const uint4 w = *reinterpret_cast<const uint4*>(
-                  base + (SUB + sub) * C::TBP + swz((uint32_t)(kr * C::RB + (hh * (CPR / 2) + c) * 16)));
+                  base + C::VOFF + sub * C::TBP + swz((uint32_t)(kr * C::RB + (hh * (CPR / 2) + c) * 16)));
               em = __vmaxu2(em, w.x & 0x7F807F80u);
               em = __vmaxu2(em, w.y & 0x7F807F80u);
               em = __vmaxu2(em, w.z & 0x7F807F80u);
@@ -492,7 +526,7 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
             const int sub = key >> 4, kr = key & 15;
             const int pos = t * WKT + key;
             const bool live = ((have >> sub) & 1u) && pos >= kmin && pos <= pmax;
-            x[k] = live ? *reinterpret_cast<const uint32_t*>(base + (SUB + sub) * C::TBP +
+            x[k] = live ? *reinterpret_cast<const uint32_t*>(base + C::VOFF + sub * C::TBP +
                                                             swz((uint32_t)(kr * C::RB + 4 * dp)))
                         : 0u;
             // 2^(14 - e) from 2^(e - 14); 2^127 for a key with no data (its values are 0)
@@ -940,6 +974,41 @@ __global__ void __launch_bounds__(WRoles<D>::THREADS, 1)
   }
 }
 
+using WsEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+WsEncodeFn ws_encode_fn() {
+  static WsEncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<WsEncodeFn>(p);
+  }
+  return fn;
+}
+
+// A BF16 layer's K buffer as a 3-D uint8 tensor [cell][64-d block][128 bytes]:
+// one box is one 64-d block of 16 consecutive cells, which lands as 16 rows
+// of the K operand (128-byte swizzle).
+bool make_kblock_map(CUtensorMap* m, const void* base, long long total_bytes, int row_bytes) {
+  WsEncodeFn fn = ws_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)(row_bytes / 128), (cuuint64_t)(total_bytes / row_bytes)};
+  cuuint64_t strides[2] = {128, (cuuint64_t)row_bytes};
+  cuuint32_t box[3] = {128, 1, 16};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MODE, int D, int G>
 cudaError_t wslaunch3(const PrefillArgs& pa0, int max_query_len, cudaStream_t st) {
   using C = WCfg<MODE, D>;
@@ -947,8 +1016,9 @@ cudaError_t wslaunch3(const PrefillArgs& pa0, int max_query_len, cudaStream_t st
   const long long total = a.num_blocks * a.Hkv * a.bs * (long long)C::RB;
   CUtensorMap km, vm;
   if (total > 0) {
-    if (!make_tile_map(&km, a.k_cache, total, C::TB) || !make_tile_map(&vm, a.v_cache, total, C::TB))
-      return cudaErrorInvalidValue;
+    const bool kok = C::KDIRECT ? make_kblock_map(&km, a.k_cache, total, C::RB)
+                                : make_tile_map(&km, a.k_cache, total, C::TB);
+    if (!kok || !make_tile_map(&vm, a.v_cache, total, C::TB)) return cudaErrorInvalidValue;
   }
   static bool attr_set[64] = {false};
   int dev = 0;

@@ -29,6 +29,16 @@ __device__ __forceinline__ void tma_tile_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// One box of a 3-D tensor map at coordinates (x, y, z) into shared memory.
+__device__ __forceinline__ void tma_tile_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // As tma_tile_2d, with an L2 eviction-priority policy (createpolicy) for
 // data read once.
 __device__ __forceinline__ void tma_tile_2d_hint(void* dst, const CUtensorMap* map, int x, int y,
