@@ -687,6 +687,7 @@ PREFILL_BLOCK = [
     ("llama8b", "fp8_per_token_head"),
     ("llama8b", "fp8_per_head"),
     ("llama8b", "int4_per_token_head"),
+    ("llama8b", "bf16"),
     ("gemma_d256", "fp8_per_token_head"),
     ("gptoss20b", "fp8_per_token_head"),
 ]
