@@ -6,7 +6,7 @@ and full layers, quantized modes (the
 warp-specialised kernel) and BF16 (the single-role kernel), with ragged
 chunks that leave the second query tile of the last CTA partly or wholly
 empty.  Each output row is checked against the oracle's prefill with the
-decode tolerance, judged as the decode of that query."""
+decode tolerance, checked as the decode of that query."""
 import pytest
 
 from int4_quantized_paged_gb300 import workloads as wl
