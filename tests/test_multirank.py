@@ -153,3 +153,18 @@ def test_layer_breakdown_reports_every_layer():
     assert rows[0]["decode_gbs"] == round(68.2e6 / 0.02e-3 / 1e9, 2)
     assert rows[1]["decode_ms"] == 0.34 and rows[1]["write_ms"] == 0.009
     json.dumps(rows)
+
+
+def test_bench_blocks_name_known_workloads_and_modes():
+    """Every configuration and prefill chunk the default bench times names a
+    workload the bench knows and a mode the library has, so the default line
+    cannot fail on a misspelt entry."""
+    from int4_quantized_paged_gb300.workloads import CONFIGS, MODES
+    assert bench.CONFIG_BLOCK and bench.PREFILL_BLOCK
+    for wname, mode, skip in bench.CONFIG_BLOCK:
+        assert wname in bench.WORKLOADS and wname in CONFIGS, wname
+        assert mode in MODES, mode
+        assert isinstance(skip, bool)
+    for wname, mode in bench.PREFILL_BLOCK:
+        assert wname in bench.PREFILL and wname in CONFIGS, wname
+        assert mode in MODES, mode
